@@ -1,0 +1,175 @@
+/*
+ * w4a16.h - C ABI of the GB300 (sm_103a) W4A16 group-quantised GEMM library
+ * (libw4a16.so).
+ *
+ * Weight format. "The Quiet Commit: How a Single Documentation Edit Marks the
+ * Completion of a Major Engineering Milestone", section "The INT4 Milestone",
+ * and section "Input Knowledge Required": symmetric per-group INT4 weights,
+ * 8 nibbles packed per int32 along the input dimension (K), stored value
+ * nibble = q + 8 (so the weight is nibble - 8), one fp32 scale per group of
+ * 32 consecutive input columns. Within a word, input column k sits in bits
+ * 4*(k mod 8) .. 4*(k mod 8)+3 (low nibble first).
+ *   qw[N][K/8]  int32   row n = output feature, K-contiguous
+ *   sc[N][K/32] float   scale of (row n, group k/32)
+ *   W_hat[n][k] = (nibble(n,k) - 8) * sc[n][k/32]
+ *
+ * Operation. "The Silence of Success: A Single Line That Speaks Volumes",
+ * section "What the Edit Actually Built": activations (fp32; a bf16 mode is
+ * the "16-bit activations" of the W4A16 name) times the INT4 weights with
+ * fp32 accumulation:  y[m][n] = sum_k x[m][k] * W_hat[n][k]  ("NT": both
+ * operands K-contiguous, y row-major fp32).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or retains them. Row-major, densely
+ *     packed (leading dimension = row length) unless stated.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     A return of W4A16_OK means the work was launched, not finished.
+ *   - Argument errors are detected on the host before any launch and return
+ *     a status without touching memory. Errors that depend on device data
+ *     (an expert id outside [0, E)) or on a bounded device-side wait that
+ *     ran out are recorded in a per-device status word; read and clear it
+ *     with w4a16_last_device_status().
+ *   - The library allocates nothing per call. The MoE entry point works in
+ *     a caller-provided workspace whose size w4a16_moe_workspace_size()
+ *     reports.
+ *   - Results are deterministic: no floating-point atomics; every sum has a
+ *     fixed order, so the same inputs give the same bits on every call.
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* same type as cudaStream_t */
+typedef struct CUstream_st *w4a16_stream_t;
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, K % 32 != 0,
+                                bad enum, workspace too small, id out of range */
+  W4A16_ERR_UNSUPPORTED = 2, /* group != 32, or a size beyond a kernel limit */
+  W4A16_ERR_ALIGNMENT = 3,   /* a pointer not 16-byte aligned */
+  W4A16_ERR_CUDA = 4,        /* a CUDA runtime or launch error */
+  W4A16_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out */
+} w4a16_status;
+
+typedef enum {
+  W4A16_ACT_F32 = 0,  /* fp32 activations: the pages' kernel */
+  W4A16_ACT_BF16 = 1  /* bf16 activations: the "A16" of W4A16 */
+} w4a16_act_dtype;
+
+/* Kernel choice for w4a16_gemm_ex (tests and tuning). */
+typedef enum {
+  W4A16_ALGO_AUTO = 0,   /* pick by M and dtype (what w4a16_gemm does) */
+  W4A16_ALGO_SIMT = 1,   /* streaming CUDA-core kernel, any M, both dtypes */
+  W4A16_ALGO_TC = 2      /* tcgen05 tensor-core kernel, bf16 activations */
+} w4a16_algo;
+
+/*
+ * w4a16_gemm - y = x * W_hat^T.
+ *   x   [M][K]   fp32 or bf16 (xdt), device, 16-byte aligned
+ *   qw  [N][K/8] int32 packed nibbles, device, 16-byte aligned
+ *   sc  [N][K/32] fp32 scales, device, 16-byte aligned
+ *   y   [M][N]   fp32 output, device, 16-byte aligned (overwritten)
+ *   group must be 32; K must be a positive multiple of 32; M, N > 0.
+ * fp32 mode keeps every output within 1e-5 * sum_k |x*W_hat| of the exact
+ * product; bf16 mode within 4e-3 of it (exact product of the bf16 values).
+ * Errors: INVALID_ARG, UNSUPPORTED (group != 32, K > 32768), ALIGNMENT, CUDA.
+ */
+w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt,
+                        const int32_t *qw, const float *sc,
+                        int M, int N, int K, int group,
+                        float *y, w4a16_stream_t stream);
+
+/* w4a16_gemm with an explicit kernel choice; W4A16_ALGO_TC requires bf16
+ * activations (UNSUPPORTED otherwise). Same arguments and errors. */
+w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt,
+                           const int32_t *qw, const float *sc,
+                           int M, int N, int K, int group,
+                           float *y, w4a16_algo algo, w4a16_stream_t stream);
+
+/* Number of kernel launches a w4a16_gemm_ex call with these arguments makes
+ * (all on `stream`, in order), or -status if the call would be rejected.
+ * Host-only; touches no device memory. */
+int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt,
+                        w4a16_algo algo);
+
+/*
+ * w4a16_quantize - the per-group symmetric INT4 quantiser (the
+ * quantize_w4a16 step of "The Quiet Commit: ... Major Engineering
+ * Milestone", section "The INT4 Milestone"), to prepare weights on the
+ * device:  s = max|w| / 7 (fp32 division), q = clamp(round-half-even(w / s),
+ * -8, 7) (q = 0 when s = 0), nibble = q + 8, packed low nibble first.
+ *   w  [N][K]    fp32 input (finite values), device
+ *   qw [N][K/8]  int32 output, device;  sc [N][K/32] fp32 output, device
+ * Errors: INVALID_ARG, UNSUPPORTED (group != 32), ALIGNMENT (qw or w not 16-byte aligned), CUDA.
+ */
+w4a16_status w4a16_quantize(const float *w, int N, int K, int group,
+                            int32_t *qw, float *sc, w4a16_stream_t stream);
+
+/*
+ * w4a16_moe_sort - group the (token, slot) pairs of a top-k routing by
+ * expert, stably. Pair p = t*topk + slot, for p in [0, n_pairs).
+ *   expert_ids [n_pairs] int32, device
+ *   offsets    [E+1] int32 output: offsets[e] = number of pairs with an
+ *              expert below e; offsets[E] = number of valid pairs
+ *   perm       [n_pairs] int32 output: pairs ordered by (expert, p)
+ * An id outside [0, E) is skipped and recorded as INVALID_ARG in the
+ * device status word. One CTA; E <= 8192.
+ */
+w4a16_status w4a16_moe_sort(const int32_t *expert_ids, int n_pairs, int E,
+                            int32_t *offsets, int32_t *perm,
+                            w4a16_stream_t stream);
+
+/* Bytes of workspace w4a16_moe_gemm needs for these sizes (either dtype). */
+size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I);
+
+/*
+ * w4a16_moe_gemm - a grouped MoE layer on INT4 experts ("The Quiet Commit:
+ * ... Major Engineering Milestone", section "The Context: A Native DDTree
+ * Engine Takes Shape" - MoE with SwiGLU - and section "The INT4 Milestone";
+ * "The Quiet Commit: How a Single Plan Update Closed Phase 3 ...", section
+ * "The Context: Phase 3 ..."):
+ *   for each token t and slot j, e = expert_ids[t][j]:
+ *     [g; u] = x[t] * W_hat_gu[e]^T   (g: rows 0..I-1, u: rows I..2I-1)
+ *     h      = silu(g) * u            (stored as bf16 in bf16 mode)
+ *     y[t]  += route_w[t][j] * (h * W_hat_dn[e]^T), slots summed in order.
+ * Tokens are sorted by expert first, so each expert's weights are streamed
+ * once per call whatever its token count.
+ *   x        [T][H] fp32 or bf16 (xdt)
+ *   expert_ids [T][topk] int32;  route_w [T][topk] fp32
+ *   qw_gu [E][2I][H/8] int32;  sc_gu [E][2I][H/32] fp32
+ *   qw_dn [E][H][I/8]  int32;  sc_dn [E][H][I/32]  fp32
+ *   workspace: device memory of at least w4a16_moe_workspace_size() bytes,
+ *   16-byte aligned, owned by the caller; contents on entry are ignored.
+ *   y [T][H] fp32 output (overwritten).
+ * group must be 32; H and I multiples of 32.
+ */
+w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt,
+                            const int32_t *expert_ids, const float *route_w,
+                            int T, int topk,
+                            const int32_t *qw_gu, const float *sc_gu,
+                            const int32_t *qw_dn, const float *sc_dn,
+                            int E, int H, int I, int group,
+                            void *workspace, size_t ws_bytes,
+                            float *y, w4a16_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *w4a16_status_string(w4a16_status s);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word (OK if no kernel recorded an error since the last call). Returns
+ * W4A16_ERR_CUDA if the synchronisation itself fails. */
+w4a16_status w4a16_last_device_status(w4a16_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

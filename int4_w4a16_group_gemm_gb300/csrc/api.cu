@@ -1,0 +1,192 @@
+// C-ABI entry points of libw4a16.so: argument validation, kernel choice and
+// the per-device status word. Declarations and contracts: include/w4a16.h.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+// Per-device status word written by kernels (first error wins).
+__device__ int g_w4a16_status;
+
+namespace w4a16 {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+
+void init_device(int dev) {
+  DeviceInfo &d = g_info[dev];
+  d.device = dev;
+  g_info_ok[dev] = false;
+  if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return;
+  if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+      cudaSuccess)
+    return;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_w4a16_status) != cudaSuccess) return;
+  d.status = static_cast<int *>(p);
+  g_info_ok[dev] = true;
+}
+}  // namespace
+
+const DeviceInfo &device_info() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(g_once[dev], init_device, dev);
+  return g_info[dev];
+}
+
+static bool device_ready() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  device_info();
+  return g_info_ok[dev];
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+static inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+static inline w4a16_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+// M at or above which bf16 activations go to the tensor-core kernel.
+static constexpr int kTcMinM = 32;
+
+// Kernel choice shared by the launch path and the launch-count query.
+// Returns OK and sets *use_tc, or the rejection status.
+static w4a16_status plan_gemm(int M, int N, int K, int group, w4a16_act_dtype xdt,
+                              w4a16_algo algo, bool *use_tc) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
+  if (algo != W4A16_ALGO_AUTO && algo != W4A16_ALGO_SIMT && algo != W4A16_ALGO_TC)
+    return W4A16_ERR_INVALID_ARG;
+  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  const bool bf16 = xdt == W4A16_ACT_BF16;
+  *use_tc = false;
+  if (algo == W4A16_ALGO_TC) {
+    if (!bf16 || !tc_gemm_supported(M, N, K)) return W4A16_ERR_UNSUPPORTED;
+    *use_tc = true;
+  } else if (algo == W4A16_ALGO_AUTO) {
+    *use_tc = bf16 && M >= kTcMinM && tc_gemm_supported(M, N, K);
+  }
+  if (!*use_tc && K > max_k_stream(1)) return W4A16_ERR_UNSUPPORTED;
+  return W4A16_OK;
+}
+
+extern "C" {
+
+int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt, w4a16_algo algo) {
+  bool use_tc = false;
+  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &use_tc);
+  if (st != W4A16_OK) return -static_cast<int>(st);
+  return use_tc ? 1 : stream_gemm_passes(M, K);
+}
+
+w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw,
+                           const float *sc, int M, int N, int K, int group, float *y,
+                           w4a16_algo algo, w4a16_stream_t stream) {
+  if (!x || !qw || !sc || !y) return W4A16_ERR_INVALID_ARG;
+  bool use_tc = false;
+  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &use_tc);
+  if (st != W4A16_OK) return st;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(sc) || !aligned16(y))
+    return W4A16_ERR_ALIGNMENT;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  const bool bf16 = xdt == W4A16_ACT_BF16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc)
+    return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y, s));
+  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N, s));
+}
+
+w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *qw, const float *sc,
+                        int M, int N, int K, int group, float *y, w4a16_stream_t stream) {
+  return w4a16_gemm_ex(x, xdt, qw, sc, M, N, K, group, y, W4A16_ALGO_AUTO, stream);
+}
+
+w4a16_status w4a16_quantize(const float *w, int N, int K, int group, int32_t *qw, float *sc,
+                            w4a16_stream_t stream) {
+  if (!w || !qw || !sc) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(qw)) return W4A16_ERR_ALIGNMENT;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  return from_cuda(launch_quantize(w, N, K, qw, sc, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_moe_sort(const int32_t *expert_ids, int n_pairs, int E, int32_t *offsets,
+                            int32_t *perm, w4a16_stream_t stream) {
+  if (!expert_ids || !offsets || !perm) return W4A16_ERR_INVALID_ARG;
+  if (n_pairs < 0 || E <= 0) return W4A16_ERR_INVALID_ARG;
+  if (E > 8192) return W4A16_ERR_UNSUPPORTED;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  return from_cuda(launch_moe_sort(expert_ids, n_pairs, E, offsets, perm,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I) {
+  if (T < 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+  return moe_workspace_bytes(T, topk, E, H, I);
+}
+
+w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *expert_ids,
+                            const float *route_w, int T, int topk, const int32_t *qw_gu,
+                            const float *sc_gu, const int32_t *qw_dn, const float *sc_dn, int E,
+                            int H, int I, int group, void *workspace, size_t ws_bytes, float *y,
+                            w4a16_stream_t stream) {
+  if (!x || !expert_ids || !route_w || !qw_gu || !sc_gu || !qw_dn || !sc_dn || !workspace || !y)
+    return W4A16_ERR_INVALID_ARG;
+  if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return W4A16_ERR_INVALID_ARG;
+  if (H % 32 != 0 || I % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
+  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  if (E > 8192 || H > max_k_stream(1) || I > max_k_stream(1)) return W4A16_ERR_UNSUPPORTED;
+  if (ws_bytes < moe_workspace_bytes(T, topk, E, H, I)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(qw_gu) || !aligned16(sc_gu) || !aligned16(qw_dn) ||
+      !aligned16(sc_dn) || !aligned16(workspace) || !aligned16(y))
+    return W4A16_ERR_ALIGNMENT;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  return from_cuda(launch_moe(x, xdt == W4A16_ACT_BF16, expert_ids, route_w, T, topk, qw_gu,
+                              sc_gu, qw_dn, sc_dn, E, H, I, workspace, y,
+                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char *w4a16_status_string(w4a16_status s) {
+  switch (s) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG";
+    case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+    case W4A16_ERR_ALIGNMENT: return "W4A16_ERR_ALIGNMENT";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+    case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+  }
+  return "W4A16_ERR_UNKNOWN";
+}
+
+w4a16_status w4a16_last_device_status(w4a16_stream_t stream) {
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  int v = 0;
+  const DeviceInfo &d = device_info();
+  if (cudaMemcpy(&v, d.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(d.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  return static_cast<w4a16_status>(v);
+}
+
+}  // extern "C"

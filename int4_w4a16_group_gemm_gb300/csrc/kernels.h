@@ -1,0 +1,56 @@
+// Internal host-side launch interface of the W4A16 kernels (not part of the
+// public C ABI; the entry points in api.cu validate arguments and call
+// these).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/w4a16.h"
+
+namespace w4a16 {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int smem_optin = 0;  // max dynamic shared memory per block (bytes)
+  int *status = nullptr;  // device address of the per-device status word
+};
+
+// Per-device facts, looked up once per device (thread-safe).
+const DeviceInfo &device_info();
+
+// ------------------------------------------------------------ streaming kernel
+// y[m0 .. m0+M) = x[m0 .. m0+M) * W_hat^T on CUDA cores, streaming the packed
+// weights once per pass of up to 4 tokens. Any M >= 1; K % 32 == 0,
+// K <= 32768. `ldx`/`ldy` are row strides in elements.
+cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
+                               const float *sc, int M, int N, int K, float *y, int ldy,
+                               cudaStream_t stream);
+// Largest K the streaming kernel accepts for a token tile of `mt` (1, 2, 4).
+int max_k_stream(int mt);
+// Token tile width the streaming kernel uses for `rem` remaining tokens.
+int stream_tile(int rem, int K);
+// Number of streaming-kernel launches for M tokens.
+int stream_gemm_passes(int M, int K);
+
+// ------------------------------------------------------------ tensor-core kernel
+// Same contract for bf16 activations on tcgen05 tensor cores.
+cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M,
+                           int N, int K, float *y, cudaStream_t stream);
+bool tc_gemm_supported(int M, int N, int K);
+
+// ------------------------------------------------------------ quantiser
+cudaError_t launch_quantize(const float *w, int N, int K, int32_t *qw, float *sc,
+                            cudaStream_t stream);
+
+// ------------------------------------------------------------ MoE
+cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *offsets,
+                            int32_t *perm, cudaStream_t stream);
+size_t moe_workspace_bytes(int T, int topk, int E, int H, int I);
+cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
+                       int T, int topk, const int32_t *qw_gu, const float *sc_gu,
+                       const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
+                       void *workspace, float *y, cudaStream_t stream);
+
+}  // namespace w4a16

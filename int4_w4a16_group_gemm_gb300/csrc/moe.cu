@@ -1,0 +1,460 @@
+// Grouped MoE layer on INT4 experts.
+//
+// "The Quiet Commit: How a Single Documentation Edit Marks the Completion of
+// a Major Engineering Milestone", section "The Context: A Native DDTree
+// Engine Takes Shape" (MoE experts with SwiGLU) and section "The INT4
+// Milestone" (experts run through the W4A16 kernel); "The Quiet Commit: How
+// a Single Plan Update Closed Phase 3 of a Native DDTree Inference Engine",
+// section "The Context: Phase 3 ..." (the INT4 W4A16 group-quantised MoE
+// path).
+//
+// Steps, all on the device and on one stream (the host reads nothing back):
+//  1. sort:     histogram of expert ids -> exclusive scan (offsets) -> stable
+//               scatter of pair indices p = t*topk + slot (perm);
+//  2. gate/up:  per expert, stream its gate and up rows once; every token of
+//               the expert multiplies them; h = silu(g) * u, stored per
+//               sorted position (bf16 in bf16 mode);
+//  3. down:     per expert, stream its down rows once; o[p] = route_w[p] *
+//               (h @ W_dn^T), stored per pair;
+//  4. combine:  y[t] = o[t*topk + 0] + o[t*topk + 1] + ... (slot order).
+// Each expert's weights are read once per call whatever its token count.
+#include <algorithm>
+
+#include "kernels.h"
+#include "stream_core.cuh"
+
+namespace w4a16 {
+
+namespace {
+
+constexpr int kMaxExperts = 8192;
+
+// ------------------------------------------------------------------ 1. sort
+__global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t *__restrict__ ids, int n,
+                                                        int E, int32_t *__restrict__ offsets,
+                                                        int32_t *__restrict__ perm, int *status) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int e = tid; e < E; e += nt) cnt[e] = 0;
+  __syncthreads();
+  for (int p = tid; p < n; p += nt) {
+    const int e = ids[p];
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[e], 1);
+    else
+      record_status(status, W4A16_ERR_INVALID_ARG);
+  }
+  __syncthreads();
+  // exclusive scan of cnt[0..E): each thread owns a contiguous chunk
+  const int per = (E + nt - 1) / nt;
+  const int b = min(E, tid * per), f = min(E, b + per);
+  int local = 0;
+  for (int e = b; e < f; ++e) local += cnt[e];
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (nt >> 5) ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - local;
+  for (int e = b; e < f; ++e) {
+    const int c = cnt[e];
+    offsets[e] = run;
+    cnt[e] = run;  // becomes the scatter cursor
+    run += c;
+  }
+  if (tid == nt - 1) offsets[E] = run;  // last thread ends at the total
+  __syncthreads();
+  // stable scatter by warp 0, 32 pairs at a time in pair order
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < n; base += 32) {
+      const int p = base + lane;
+      const bool in = p < n;
+      int e = in ? ids[p] : -1;
+      const bool valid = in && e >= 0 && e < E;
+      if (!valid) e = -1 - lane;  // unique key: never matches a valid id
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      int pos = 0;
+      if (valid) pos = cnt[e] + __popc(peers & lt);
+      __syncwarp();
+      if (valid) {
+        perm[pos] = p;
+        if ((peers & lt) == 0) cnt[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// --------------------------------------------------------- 2./3. expert GEMMs
+struct MoeParams {
+  const void *x;        // gate/up: tokens [T][H]; down: h [n][I] (sorted order)
+  const int32_t *perm;  // sorted position -> pair
+  const int32_t *offsets;
+  const float *route_w;  // [n]
+  const int32_t *qw;     // expert-major packed weights
+  const float *sc;
+  void *out;             // gate/up: h [n][I]; down: o [n][H] fp32 (by pair)
+  int H, I, topk;
+  int nstages;
+  int sc_bulk;
+  int *status;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// MODE 0: gate/up + SwiGLU (K = H, 4 gate rows + 4 up rows per stage).
+// MODE 1: down + routing weight (K = I, 8 rows per stage).
+template <int MT, bool BF16, int MODE>
+__global__ void __launch_bounds__(MT == 1 ? 1024 : 512, 1) moe_stream_kernel(const MoeParams p) {
+  constexpr int WPL = 4 / MT;
+  constexpr int EPL = 8 * WPL;
+  constexpr int SLICE = 32 * EPL;
+  constexpr int RC = kRowsPerChunk;
+  constexpr int RL = MODE == 0 ? 4 : 8;  // logical output rows per stage
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+
+  const int e = blockIdx.y;
+  const int s0 = p.offsets[e];
+  const int ce = p.offsets[e + 1] - s0;
+  if (ce <= 0) return;
+
+  const int K = MODE == 0 ? p.H : p.I;
+  const int L = MODE == 0 ? p.I : p.H;  // logical rows of the expert
+  const int nlc = (L + RL - 1) / RL;
+  const int c_begin = static_cast<int>((static_cast<long long>(nlc) * blockIdx.x) / gridDim.x);
+  const int c_end = static_cast<int>((static_cast<long long>(nlc) * (blockIdx.x + 1)) / gridDim.x);
+  const int nchunks = c_end - c_begin;
+  if (nchunks <= 0) return;
+
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = K >> 5;
+  const uint32_t qrow = static_cast<uint32_t>(K) >> 1;
+  const uint32_t srow = static_cast<uint32_t>(K) >> 3;
+  const uint32_t qstage = RC * qrow;
+  const uint32_t stage_bytes = qstage + (p.sc_bulk ? RC * srow : 0u);
+  const int NS = p.nstages;
+  const size_t erows = MODE == 0 ? 2 * static_cast<size_t>(p.I) : static_cast<size_t>(p.H);
+  const uint8_t *qbase = reinterpret_cast<const uint8_t *>(p.qw) + e * erows * qrow;
+  const uint8_t *sbase = reinterpret_cast<const uint8_t *>(p.sc) + e * erows * srow;
+
+  uint8_t *stages = smem;
+  float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * nw * RC * MT);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // global row of stage row r for logical chunk starting at l0 (-1: none)
+  auto stage_row = [&](int l0, int r) -> int {
+    if (MODE == 0) {
+      const int j = l0 + (r & 3);
+      if (j >= p.I) return -1;
+      return r < 4 ? j : p.I + j;
+    } else {
+      const int n = l0 + r;
+      return n < p.H ? n : -1;
+    }
+  };
+
+  int issued = 0;
+  auto issue = [&](int c) {
+    const int slot = c % NS;
+    const int l0 = (c_begin + c) * RL;
+    const int rows = min(RL, L - l0);
+    uint8_t *dst = stages + slot * stage_bytes;
+    const int parts = MODE == 0 ? 2 : 1;
+    const uint32_t bq = rows * qrow, bs = p.sc_bulk ? rows * srow : 0u;
+    mbar_arrive_expect_tx(&full[slot], parts * (bq + bs));
+    for (int h = 0; h < parts; ++h) {
+      const size_t grow = static_cast<size_t>(l0) + (h ? p.I : 0);
+      bulk_g2s(dst + h * 4 * qrow, qbase + grow * qrow, bq, &full[slot]);
+      if (p.sc_bulk) bulk_g2s(dst + qstage + h * 4 * srow, sbase + grow * srow, bs, &full[slot]);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (; issued < min(NS, nchunks); ++issued) issue(issued);
+
+  const int k0 = warp * SLICE + lane * EPL;
+  const bool active = k0 < K;
+  const int g = k0 >> 5;
+  const int ntiles = (ce + MT - 1) / MT;
+
+  float xr[MT][EPL];
+  auto load_tile = [&](int tile) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const int q = tile * MT + t;
+      const void *row = nullptr;
+      if (active && q < ce) {
+        const int s = s0 + q;
+        if (MODE == 0) {
+          const int tok = p.perm[s] / p.topk;
+          row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
+                                                 static_cast<size_t>(tok) * p.H)
+                     : static_cast<const void *>(static_cast<const float *>(p.x) +
+                                                 static_cast<size_t>(tok) * p.H);
+        } else {
+          row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
+                                                 static_cast<size_t>(s) * p.I)
+                     : static_cast<const void *>(static_cast<const float *>(p.x) +
+                                                 static_cast<size_t>(s) * p.I);
+        }
+      }
+      load_x_slice<EPL, BF16>(row, k0, xr[t]);
+    }
+  };
+  if (ntiles == 1) load_tile(0);
+
+  int it = 0;  // reduction-buffer parity across chunks and tiles
+  int c = 0;
+  for (; c < nchunks; ++c) {
+    const int slot = c % NS;
+    const int l0 = (c_begin + c) * RL;
+    const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>(c / NS) & 1u);
+    if (!ok) {
+      record_status(p.status, W4A16_ERR_TIMEOUT);
+      s_abort = 1;
+    }
+    const uint8_t *st = stages + slot * stage_bytes;
+    bool abort = false;
+    for (int tile = 0; tile < ntiles; ++tile, ++it) {
+      if (ntiles > 1) load_tile(tile);
+      float part[RC][MT];
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        const int grow = stage_row(l0, r);
+        float acc[MT];
+        if (ok && active && grow >= 0) {
+          uint32_t wd[WPL];
+          load_words<WPL>(st + r * qrow + (k0 >> 1), wd);
+          const float s = p.sc_bulk
+                              ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
+                              : __ldg(reinterpret_cast<const float *>(sbase) +
+                                      static_cast<size_t>(grow) * G + g);
+          lane_dot<MT, WPL>(wd, xr, acc);
+#pragma unroll
+          for (int t = 0; t < MT; ++t) part[r][t] = acc[t] * s;
+        } else {
+#pragma unroll
+          for (int t = 0; t < MT; ++t) part[r][t] = 0.f;
+        }
+      }
+      float res[MT];
+      warp_reduce_8rows<MT>(part, res, lane);
+      float *redb = red + (it & 1) * nw * RC * MT;
+      if ((lane & 3) == 0) {
+        const int row = (lane >> 2) & 7;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) redb[(warp * RC + row) * MT + t] = res[t];
+      }
+      named_bar_sync(1, blockDim.x);
+      abort = s_abort != 0;
+      if (abort) break;
+      if (MODE == 0) {
+        if (threadIdx.x < 4 * MT) {
+          const int jj = threadIdx.x / MT, t = threadIdx.x % MT;
+          const int q = tile * MT + t;
+          if (l0 + jj < p.I && q < ce) {
+            float gs = redb[jj * MT + t], us = redb[(4 + jj) * MT + t];
+            for (int w = 1; w < nw; ++w) {
+              gs += redb[(w * RC + jj) * MT + t];
+              us += redb[(w * RC + 4 + jj) * MT + t];
+            }
+            const float h = silu_f(gs) * us;
+            const size_t idx = static_cast<size_t>(s0 + q) * p.I + l0 + jj;
+            if (BF16)
+              static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
+            else
+              static_cast<float *>(p.out)[idx] = h;
+          }
+        }
+      } else {
+        if (threadIdx.x < RC * MT) {
+          const int row = threadIdx.x / MT, t = threadIdx.x % MT;
+          const int q = tile * MT + t;
+          if (l0 + row < p.H && q < ce) {
+            float v = redb[row * MT + t];
+            for (int w = 1; w < nw; ++w) v += redb[(w * RC + row) * MT + t];
+            const int pair = p.perm[s0 + q];
+            static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + row] =
+                p.route_w[pair] * v;
+          }
+        }
+      }
+    }
+    if (abort) break;
+    // every thread passed the last barrier of this chunk: the slot is free
+    if (threadIdx.x == 0 && issued < nchunks) {
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (threadIdx.x == 0 && c < nchunks) {
+    for (int d = c; d < issued; ++d) mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+  }
+}
+
+// ------------------------------------------------------------------ 4. combine
+__global__ void moe_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
+                                   int T, int topk, int H, int E, float *__restrict__ y) {
+  const int H4 = H >> 2;
+  const long long total = static_cast<long long>(T) * H4;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / H4);
+    const int n4 = static_cast<int>(i % H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < topk; ++j) {
+      const int pair = t * topk + j;
+      const int e = ids[pair];
+      if (e < 0 || e >= E) continue;
+      const float4 v = reinterpret_cast<const float4 *>(o + static_cast<size_t>(pair) * H)[n4];
+      if (j == 0) {
+        acc = v;
+      } else {
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+    }
+    reinterpret_cast<float4 *>(y + static_cast<size_t>(t) * H)[n4] = acc;
+  }
+}
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t off_offsets, off_perm, off_h, off_o, total;
+};
+
+WsLayout ws_layout(int T, int topk, int E, int H, int I) {
+  const size_t n = static_cast<size_t>(T) * topk;
+  WsLayout w{};
+  w.off_offsets = 0;
+  w.off_perm = align256(sizeof(int32_t) * (E + 1));
+  w.off_h = w.off_perm + align256(sizeof(int32_t) * std::max<size_t>(n, 1));
+  w.off_o = w.off_h + align256(sizeof(float) * n * I);
+  w.total = w.off_o + align256(sizeof(float) * n * H);
+  return w;
+}
+
+template <int MT, bool BF16, int MODE>
+cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
+                               cudaStream_t stream) {
+  constexpr int SLICE = 32 * 8 * (4 / MT);
+  const int nw = (K + SLICE - 1) / SLICE;
+  const int threads = nw * 32;
+  const uint32_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
+  const size_t fixed = 2ull * nw * kRowsPerChunk * MT * sizeof(float) + 64;
+  const size_t budget = static_cast<size_t>(di.smem_optin) - 1024;
+  int ns = 4;
+  while (ns > 1 && fixed + static_cast<size_t>(ns) * stage > budget) --ns;
+  if (fixed + static_cast<size_t>(ns) * stage > budget) return cudaErrorInvalidConfiguration;
+  p.nstages = ns;
+  const size_t smem = fixed + static_cast<size_t>(ns) * stage;
+  auto kern = moe_stream_kernel<MT, BF16, MODE>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  // split every expert into several CTAs so the active experts spread
+  // evenly over the SMs (empty experts exit at once)
+  const int per_expert = 8;
+  dim3 grid(per_expert, E);
+  kern<<<grid, threads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_expert(MoeParams p, bool bf16, int K, int E, const DeviceInfo &di,
+                          cudaStream_t stream) {
+  p.sc_bulk = (K % 128 == 0) ? 1 : 0;
+  if (K <= max_k_stream(4))
+    return bf16 ? launch_expert_pass<4, true, MODE>(p, K, E, di, stream)
+                : launch_expert_pass<4, false, MODE>(p, K, E, di, stream);
+  if (K <= max_k_stream(2))
+    return bf16 ? launch_expert_pass<2, true, MODE>(p, K, E, di, stream)
+                : launch_expert_pass<2, false, MODE>(p, K, E, di, stream);
+  return bf16 ? launch_expert_pass<1, true, MODE>(p, K, E, di, stream)
+              : launch_expert_pass<1, false, MODE>(p, K, E, di, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *offsets,
+                            int32_t *perm, cudaStream_t stream) {
+  const DeviceInfo &di = device_info();
+  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n_pairs, E, offsets, perm, di.status);
+  return cudaGetLastError();
+}
+
+size_t moe_workspace_bytes(int T, int topk, int E, int H, int I) {
+  return ws_layout(T, topk, E, H, I).total;
+}
+
+cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
+                       int T, int topk, const int32_t *qw_gu, const float *sc_gu,
+                       const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
+                       void *workspace, float *y, cudaStream_t stream) {
+  const DeviceInfo &di = device_info();
+  const WsLayout L = ws_layout(T, topk, E, H, I);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.off_offsets);
+  int32_t *perm = reinterpret_cast<int32_t *>(ws + L.off_perm);
+  void *h = ws + L.off_h;
+  float *o = reinterpret_cast<float *>(ws + L.off_o);
+  const int n = T * topk;
+
+  cudaError_t err = launch_moe_sort(ids, n, E, offsets, perm, stream);
+  if (err != cudaSuccess) return err;
+
+  MoeParams p{};
+  p.perm = perm;
+  p.offsets = offsets;
+  p.route_w = route_w;
+  p.H = H;
+  p.I = I;
+  p.topk = topk;
+  p.status = di.status;
+
+  p.x = x;
+  p.qw = qw_gu;
+  p.sc = sc_gu;
+  p.out = h;
+  err = launch_expert<0>(p, x_bf16, H, E, di, stream);
+  if (err != cudaSuccess) return err;
+
+  p.x = h;
+  p.qw = qw_dn;
+  p.sc = sc_dn;
+  p.out = o;
+  err = launch_expert<1>(p, x_bf16, I, E, di, stream);
+  if (err != cudaSuccess) return err;
+
+  const long long work = static_cast<long long>(T) * (H / 4);
+  const int grid = static_cast<int>(std::min<long long>((work + 255) / 256, di.num_sms * 8ll));
+  moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, T, topk, H, E, y);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

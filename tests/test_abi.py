@@ -1,0 +1,86 @@
+"""The C-ABI library loads and exports every entry point include/w4a16.h
+declares; host-side argument checks return their status codes without a
+GPU (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import int4_w4a16_group_gemm_gb300 as w4
+    return w4
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["w4a16_gemm", "w4a16_gemm_ex", "w4a16_quantize", "w4a16_moe_sort",
+              "w4a16_moe_workspace_size", "w4a16_moe_gemm", "w4a16_status_string",
+              "w4a16_last_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(w4):
+    lib = ctypes.CDLL(w4.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} not exported"
+    # the binding wraps every declared function with a signature
+    assert set(declared_functions()) <= set(w4.SIGNATURES)
+
+
+def test_status_strings(w4):
+    assert w4.status_string(0) == "W4A16_OK"
+    assert w4.status_string(5) == "W4A16_ERR_TIMEOUT"
+    assert w4.status_string(99) == "W4A16_ERR_UNKNOWN"
+
+
+def test_host_argument_checks_need_no_gpu(w4):
+    lib = w4.lib
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)       # never dereferenced: checks fail first
+    odd = ctypes.c_void_p(0x1004)
+    # null pointers
+    assert lib.w4a16_gemm(null, 0, fake, fake, 1, 1, 32, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    # sizes
+    assert lib.w4a16_gemm(fake, 0, fake, fake, 0, 1, 32, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 48, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    # group size other than 32
+    assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 64, 64, fake, null) == w4.W4A16_ERR_UNSUPPORTED
+    # bad activation dtype
+    assert lib.w4a16_gemm(fake, 7, fake, fake, 1, 1, 32, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    # misaligned operand
+    assert lib.w4a16_gemm(odd, 0, fake, fake, 1, 1, 32, 32, fake, null) == w4.W4A16_ERR_ALIGNMENT
+    # bad algo
+    assert lib.w4a16_gemm_ex(fake, 0, fake, fake, 1, 1, 32, 32, fake, 9, null) == w4.W4A16_ERR_INVALID_ARG
+    # quantiser
+    assert lib.w4a16_quantize(null, 4, 32, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_quantize(fake, 4, 40, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    # sort
+    assert lib.w4a16_moe_sort(fake, 4, 0, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_sort(fake, 4, 9000, fake, fake, null) == w4.W4A16_ERR_UNSUPPORTED
+    # MoE: workspace too small
+    ws = w4.w4a16_moe_workspace_size(4, 2, 3, 64, 64)
+    assert lib.w4a16_moe_gemm(fake, 1, fake, fake, 4, 2, fake, fake, fake, fake, 3, 64, 64, 32,
+                              fake, max(ws - 1, 0), fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_gemm(fake, 1, fake, fake, 4, 2, fake, fake, fake, fake, 3, 64, 48, 32,
+                              fake, ws, fake, null) == w4.W4A16_ERR_INVALID_ARG
+
+
+def test_workspace_size_grows_with_tokens(w4):
+    a = w4.w4a16_moe_workspace_size(128, 8, 384, 7168, 2048)
+    b = w4.w4a16_moe_workspace_size(256, 8, 384, 7168, 2048)
+    assert 0 < a < b
+    assert w4.w4a16_moe_workspace_size(-1, 8, 384, 7168, 2048) == 0

@@ -1,0 +1,147 @@
+"""Parity of the CUDA W4A16 GEMM with the CPU oracle, through the C ABI.
+
+Each case draws x and W from the seeded generators, quantises W twice - on
+the device with w4a16_quantize and on the host with the oracle's quantiser -
+checks the two packings are bit-identical, then compares every output of
+the device GEMM with the oracle's fp64 product:
+  fp32 activations: |y - y_ref| <= 1e-5 * sum_k |x * W_hat|
+  bf16 activations: |y - y_ref| <= 4e-3 * sum_k |x * W_hat| (oracle fed the
+  same bf16 values).
+Workload shapes: the tiny GEMM (1x256 -> 512), the decode GEMV (1x7168 ->
+4096), the tree-verify pair (64x7168 -> 4096 and 64x2048 -> 7168, 1 % of
+activations x20), the prefill GEMM (2048x7168 -> 18432, checked on sampled
+rows) and ragged edge cases.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 4e-3}
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import int4_w4a16_group_gemm_gb300 as w4
+    return w4
+
+
+def quantize_both(w4, w):
+    """Device quantiser and oracle quantiser on the same W; must agree bit-exactly."""
+    wd = torch.from_numpy(w).cuda()
+    qw_d, sc_d = w4.w4a16_quantize(wd)
+    qw_h, sc_h = oracle.quantize_w4a16(w)
+    np.testing.assert_array_equal(qw_d.cpu().numpy(), qw_h)
+    np.testing.assert_array_equal(sc_d.cpu().numpy().view(np.uint32), sc_h.view(np.uint32))
+    return qw_d, sc_d, qw_h, sc_h
+
+
+def run_case(w4, M, N, K, dt, seed=0, outlier=0.0, algo="auto", rows=None):
+    x = synth.activations(seed, M, K, outlier_frac=outlier)
+    w = synth.weights(seed, N, K)
+    qw_d, sc_d, qw_h, sc_h = quantize_both(w4, w)
+    xt = torch.from_numpy(x)
+    if dt == "bf16":
+        xt = xt.to(torch.bfloat16)
+    y = w4.w4a16_gemm(xt.cuda(), qw_d, sc_d, algo=algo)
+    torch.cuda.synchronize()
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    yh = y.cpu().numpy().astype(np.float64)
+    xo = xt.float().numpy()
+    if rows is not None:
+        xo = xo[rows]
+        yh = yh[rows]
+    ref, bound = oracle.gemm_ref(xo, qw_h, sc_h)
+    err = np.abs(yh - ref)
+    ratio = np.max(err / np.maximum(bound, 1e-300))
+    assert np.all(err <= TOL[dt] * bound), f"max err/bound = {ratio:.3e}"
+    return y, ratio
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_tiny_gemm(w4, dt):
+    run_case(w4, 1, 512, 256, dt)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_decode_gemv(w4, dt):
+    run_case(w4, 1, 4096, 7168, dt, seed=1)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(4096, 7168), (7168, 2048)])
+def test_tree_verify_pair(w4, dt, shape):
+    N, K = shape
+    run_case(w4, 64, N, K, dt, seed=2, outlier=0.01)
+
+
+@pytest.mark.parametrize("algo", ["simt"])
+def test_tree_verify_forced_simt(w4, algo):
+    run_case(w4, 64, 4096, 7168, "bf16", seed=3, outlier=0.01, algo=algo)
+
+
+def test_prefill_gemm_sampled_rows(w4):
+    M, N, K = 2048, 18432, 7168
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(M, size=48, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    run_case(w4, M, N, K, "bf16", seed=4, rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 32), (2, 13, 96), (3, 1000, 160), (5, 37, 4128), (7, 8, 1024),
+    (4, 100, 8192), (3, 24, 8224), (2, 9, 16384), (1, 5, 32768), (9, 33, 256),
+])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_ragged_shapes(w4, M, N, K, dt):
+    run_case(w4, M, N, K, dt, seed=M * 1000 + N)
+
+
+def test_degenerate_weights_and_activations(w4):
+    M, N, K = 3, 16, 256
+    # all nibbles 0 (q = -8), unit scales: y = -8 * sum_k x exactly representable
+    nib = np.zeros((N, K), np.int64)
+    qw = oracle.pack_nibbles(nib)
+    sc = np.ones((N, K // 32), np.float32)
+    x = np.ones((M, K), np.float32)
+    y = w4.w4a16_gemm(torch.from_numpy(x).cuda(), torch.from_numpy(qw).cuda(),
+                      torch.from_numpy(sc).cuda())
+    assert (y.cpu().numpy() == -8.0 * K).all()
+    # zero activations give exact zeros; zero scales too
+    x0 = np.zeros((M, K), np.float32)
+    w = synth.weights(9, N, K)
+    qw2, sc2 = oracle.quantize_w4a16(w)
+    y0 = w4.w4a16_gemm(torch.from_numpy(x0).cuda(), torch.from_numpy(qw2).cuda(),
+                       torch.from_numpy(sc2).cuda())
+    assert (y0.cpu().numpy() == 0).all()
+    y1 = w4.w4a16_gemm(torch.from_numpy(synth.activations(9, M, K)).cuda(),
+                       torch.from_numpy(qw2).cuda(), torch.zeros_like(torch.from_numpy(sc2)).cuda())
+    assert (y1.cpu().numpy() == 0).all()
+
+
+def test_deterministic_bits(w4):
+    M, N, K = 5, 777, 7168
+    x = torch.from_numpy(synth.activations(5, M, K)).cuda()
+    qw, sc = w4.w4a16_quantize(torch.from_numpy(synth.weights(5, N, K)).cuda())
+    a = w4.w4a16_gemm(x, qw, sc)
+    b = w4.w4a16_gemm(x, qw, sc)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_gemm_on_side_stream(w4):
+    M, N, K = 2, 300, 2048
+    x = torch.from_numpy(synth.activations(6, M, K)).cuda()
+    qw, sc = w4.w4a16_quantize(torch.from_numpy(synth.weights(6, N, K)).cuda())
+    ref = w4.w4a16_gemm(x, qw, sc)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = w4.w4a16_gemm(x, qw, sc, stream=s)
+    s.synchronize()
+    assert torch.equal(y, ref)
