@@ -170,13 +170,14 @@ def _rotation(bytes_per_copy, l2_bytes):
 
 class GemmWorkload(Workload):
     def __init__(self, w4, torch, dev, M, N, K, dtype, seed, name, outlier=0.0, algo="auto",
-                 l2_bytes=129 * 2 ** 20):
+                 l2_bytes=129 * 2 ** 20, overlap=True):
         import synth
         self.w4, self.torch, self.dev = w4, torch, dev
         self.M, self.N, self.K = M, N, K
         self.dtype = dtype
         self.name = name
         self.algo = algo
+        self.overlap = overlap
         wbytes = N * K // 2 + N * (K // 32) * 4
         xb = M * K * (2 if dtype == "bf16" else 4)
         self.bytes = wbytes + xb + M * N * 4
@@ -211,12 +212,14 @@ class GemmWorkload(Workload):
 
     def step(self, i, stream):
         c = i % self.ncopies
-        self.w4.w4a16_gemm(self.x, self.qw[c], self.sc[c], y=self.y, algo=self.algo, stream=stream)
+        self.w4.w4a16_gemm(self.x, self.qw[c], self.sc[c], y=self.y, algo=self.algo,
+                           overlap=self.overlap, stream=stream)
 
     def e2e_step(self, i, stream):
         c = i % self.ncopies
         self.x.copy_(self.x_host, non_blocking=True)
-        self.w4.w4a16_gemm(self.x, self.qw[c], self.sc[c], y=self.y, algo=self.algo, stream=stream)
+        self.w4.w4a16_gemm(self.x, self.qw[c], self.sc[c], y=self.y, algo=self.algo,
+                           overlap=self.overlap, stream=stream)
         self.y_host.copy_(self.y, non_blocking=True)
         stream.synchronize()
 
@@ -360,12 +363,14 @@ class MoeWorkload(Workload):
                                           f"({len(experts)} experts), scaled by token-slots")
 
 
-def make_workload(cfg, dtype, w4, torch, dev):
+def make_workload(cfg, dtype, w4, torch, dev, overlap=True):
     if cfg == 0:
-        return GemmWorkload(w4, torch, dev, 1, 512, 256, "f32", 0, "tiny GEMM M=1 K=256 N=512 fp32")
+        return GemmWorkload(w4, torch, dev, 1, 512, 256, "f32", 0, "tiny GEMM M=1 K=256 N=512 fp32",
+                            overlap=overlap)
     if cfg == 1:
         return GemmWorkload(w4, torch, dev, 1, 4096, 7168, "f32", 0,
-                            "decode GEMV M=1 K=7168 N=4096 group=32 fp32 activations")
+                            "decode GEMV M=1 K=7168 N=4096 group=32 fp32 activations",
+                            overlap=overlap)
     if cfg == 2:
         return TreeVerifyWorkload(w4, torch, dev, dtype)
     if cfg == 3:
@@ -445,7 +450,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     import int4_w4a16_group_gemm_gb300 as w4
 
-    wl = make_workload(args.config, args.dtype, w4, torch, dev)
+    wl = make_workload(args.config, args.dtype, w4, torch, dev, overlap=not args.no_overlap)
     stream = torch.cuda.Stream(device=dev)
     pk = peaks()
 
@@ -540,6 +545,7 @@ def run_ours(args):
                    "l2": (f"{getattr(wl, 'ncopies', 1)} rotating weight copies (> 4x L2)"
                           if getattr(wl, "ncopies", 1) > 1 else "working set larger than L2"),
                    "timing": "one CUDA graph of K steps" if graph is not None else "eager launches",
+                   "overlap": bool(getattr(wl, "overlap", False)),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
@@ -568,6 +574,8 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="bf16")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch without programmatic dependent launch (W4A16_FLAG_OVERLAP)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=2000)

@@ -87,12 +87,26 @@ w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt,
                         int M, int N, int K, int group,
                         float *y, w4a16_stream_t stream);
 
-/* w4a16_gemm with an explicit kernel choice; W4A16_ALGO_TC requires bf16
- * activations (UNSUPPORTED otherwise). Same arguments and errors. */
+/* Launch options for w4a16_gemm_ex (bit flags). */
+enum {
+  /* Overlap with the previous kernel on the stream (programmatic dependent
+   * launch): the call may begin streaming qw/sc while the kernel launched
+   * just before it is still running; it reads x and writes y only after
+   * that kernel has completed. The caller guarantees that the kernel
+   * launched just before does not write qw or sc (true when weights are
+   * prepared earlier, as in a decode loop). Used by the streaming kernel;
+   * ignored by the tensor-core kernel. */
+  W4A16_FLAG_OVERLAP = 1u
+};
+
+/* w4a16_gemm with an explicit kernel choice and launch flags (0 = none);
+ * W4A16_ALGO_TC requires bf16 activations (UNSUPPORTED otherwise). Same
+ * arguments and errors as w4a16_gemm, plus INVALID_ARG for unknown flags. */
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt,
                            const int32_t *qw, const float *sc,
                            int M, int N, int K, int group,
-                           float *y, w4a16_algo algo, w4a16_stream_t stream);
+                           float *y, w4a16_algo algo, unsigned int flags,
+                           w4a16_stream_t stream);
 
 /* Number of kernel launches a w4a16_gemm_ex call with these arguments makes
  * (all on `stream`, in order), or -status if the call would be rejected.

@@ -35,12 +35,13 @@ ACT_F32 = 0
 ACT_BF16 = 1
 
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+FLAG_OVERLAP = 1
 
 # name -> (restype, argtypes), mirroring include/w4a16.h
 _VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "w4a16_gemm": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
-    "w4a16_gemm_ex": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _I, _VP, _I, _VP]),
+    "w4a16_gemm_ex": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _I, _VP, _I, ctypes.c_uint, _VP]),
     "w4a16_gemm_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "w4a16_quantize": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP]),
     "w4a16_moe_sort": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
@@ -115,8 +116,13 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def w4a16_gemm(x, qw, sc, y=None, group: int = 32, algo: str = "auto", stream=None):
-    """y[M, N] = x[M, K] @ W_hat[N, K]^T via the C ABI."""
+def w4a16_gemm(x, qw, sc, y=None, group: int = 32, algo: str = "auto", overlap: bool = False,
+               stream=None):
+    """y[M, N] = x[M, K] @ W_hat[N, K]^T via the C ABI.
+
+    overlap=True sets W4A16_FLAG_OVERLAP: the weight stream may start while
+    the previous kernel on the stream is still running (the caller promises
+    that kernel does not write qw or sc)."""
     import torch
     xdt = _act_dtype(x)
     _need(x, x.dtype, "x")
@@ -128,7 +134,7 @@ def w4a16_gemm(x, qw, sc, y=None, group: int = 32, algo: str = "auto", stream=No
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _need(y, torch.float32, "y")
     code = lib.w4a16_gemm_ex(_ptr(x), xdt, _ptr(qw), _ptr(sc), M, N, K, group, _ptr(y),
-                             ALGOS[algo], _stream_handle(stream))
+                             ALGOS[algo], FLAG_OVERLAP if overlap else 0, _stream_handle(stream))
     _check("w4a16_gemm", code)
     return y
 
@@ -140,11 +146,12 @@ def w4a16_gemm_launches(M: int, N: int, K: int, dtype: str = "f32", algo: str = 
                                        ALGOS[algo]))
 
 
-def w4a16_gemm_raw(x_ptr, xdt, qw_ptr, sc_ptr, M, N, K, group, y_ptr, algo=0, stream_ptr=0):
+def w4a16_gemm_raw(x_ptr, xdt, qw_ptr, sc_ptr, M, N, K, group, y_ptr, algo=0, flags=0,
+                   stream_ptr=0):
     """Pointer-level call (host code that manages its own buffers)."""
     return lib.w4a16_gemm_ex(ctypes.c_void_p(x_ptr), xdt, ctypes.c_void_p(qw_ptr),
                              ctypes.c_void_p(sc_ptr), M, N, K, group, ctypes.c_void_p(y_ptr),
-                             algo, ctypes.c_void_p(stream_ptr))
+                             algo, flags, ctypes.c_void_p(stream_ptr))
 
 
 def w4a16_quantize(w, group: int = 32, qw=None, sc=None, stream=None):

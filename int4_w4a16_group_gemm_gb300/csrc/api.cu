@@ -96,8 +96,9 @@ int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt, w4a
 
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw,
                            const float *sc, int M, int N, int K, int group, float *y,
-                           w4a16_algo algo, w4a16_stream_t stream) {
+                           w4a16_algo algo, unsigned int flags, w4a16_stream_t stream) {
   if (!x || !qw || !sc || !y) return W4A16_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned int>(W4A16_FLAG_OVERLAP)) return W4A16_ERR_INVALID_ARG;
   bool use_tc = false;
   const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &use_tc);
   if (st != W4A16_OK) return st;
@@ -108,12 +109,13 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc)
     return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y, s));
-  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N, s));
+  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N,
+                                      (flags & W4A16_FLAG_OVERLAP) != 0, s));
 }
 
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *qw, const float *sc,
                         int M, int N, int K, int group, float *y, w4a16_stream_t stream) {
-  return w4a16_gemm_ex(x, xdt, qw, sc, M, N, K, group, y, W4A16_ALGO_AUTO, stream);
+  return w4a16_gemm_ex(x, xdt, qw, sc, M, N, K, group, y, W4A16_ALGO_AUTO, 0u, stream);
 }
 
 w4a16_status w4a16_quantize(const float *w, int N, int K, int group, int32_t *qw, float *sc,

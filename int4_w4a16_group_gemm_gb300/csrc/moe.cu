@@ -121,9 +121,8 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 
 // MODE 0: gate/up + SwiGLU (K = H, 4 gate rows + 4 up rows per stage).
 // MODE 1: down + routing weight (K = I, 8 rows per stage).
-template <int MT, bool BF16, int MODE>
-__global__ void __launch_bounds__(MT == 1 ? 1024 : 512, 1) moe_stream_kernel(const MoeParams p) {
-  constexpr int WPL = 4 / MT;
+template <int MT, int WPL, bool BF16, int MODE>
+__global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(const MoeParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
@@ -359,10 +358,10 @@ WsLayout ws_layout(int T, int topk, int E, int H, int I) {
   return w;
 }
 
-template <int MT, bool BF16, int MODE>
+template <int MT, int WPL, bool BF16, int MODE>
 cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
                                cudaStream_t stream) {
-  constexpr int SLICE = 32 * 8 * (4 / MT);
+  constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
   const int threads = nw * 32;
   const uint32_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
@@ -373,7 +372,7 @@ cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
   if (fixed + static_cast<size_t>(ns) * stage > budget) return cudaErrorInvalidConfiguration;
   p.nstages = ns;
   const size_t smem = fixed + static_cast<size_t>(ns) * stage;
-  auto kern = moe_stream_kernel<MT, BF16, MODE>;
+  auto kern = moe_stream_kernel<MT, WPL, BF16, MODE>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -390,13 +389,10 @@ cudaError_t launch_expert(MoeParams p, bool bf16, int K, int E, const DeviceInfo
                           cudaStream_t stream) {
   p.sc_bulk = (K % 128 == 0) ? 1 : 0;
   if (K <= max_k_stream(4))
-    return bf16 ? launch_expert_pass<4, true, MODE>(p, K, E, di, stream)
-                : launch_expert_pass<4, false, MODE>(p, K, E, di, stream);
-  if (K <= max_k_stream(2))
-    return bf16 ? launch_expert_pass<2, true, MODE>(p, K, E, di, stream)
-                : launch_expert_pass<2, false, MODE>(p, K, E, di, stream);
-  return bf16 ? launch_expert_pass<1, true, MODE>(p, K, E, di, stream)
-              : launch_expert_pass<1, false, MODE>(p, K, E, di, stream);
+    return bf16 ? launch_expert_pass<4, 2, true, MODE>(p, K, E, di, stream)
+                : launch_expert_pass<4, 2, false, MODE>(p, K, E, di, stream);
+  return bf16 ? launch_expert_pass<1, 4, true, MODE>(p, K, E, di, stream)
+              : launch_expert_pass<1, 4, false, MODE>(p, K, E, di, stream);
 }
 
 }  // namespace

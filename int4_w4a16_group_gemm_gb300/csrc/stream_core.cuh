@@ -25,6 +25,10 @@ namespace w4a16 {
 
 constexpr int kRowsPerChunk = 8;
 
+// Thread budget of a streaming CTA for a token tile of MT: 1024 threads (64
+// registers each) for MT <= 2, 512 (128 registers) for MT = 4.
+__host__ __device__ constexpr int stream_max_threads(int MT) { return MT == 4 ? 512 : 1024; }
+
 __device__ __forceinline__ float nib_bias(int c) {
   // 2^23 + 8 * 16^c, exact in fp32 for c = 0..3
   return c == 0 ? 8388616.0f : c == 1 ? 8388736.0f : c == 2 ? 8390656.0f : 8421376.0f;

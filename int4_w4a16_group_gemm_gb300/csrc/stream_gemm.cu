@@ -37,14 +37,9 @@ struct StreamParams {
   int *status;
 };
 
-// Largest CTA per token-tile width: one warp per K slice, registers capped
-// by the launch bound (MT = 1: 64 per thread; MT = 2, 4: 128 per thread).
-template <int MT>
-constexpr int max_threads() { return MT == 1 ? 1024 : 512; }
-
-template <int MT, bool BF16>
-__global__ void __launch_bounds__(max_threads<MT>(), 1) stream_gemm_kernel(const StreamParams p) {
-  constexpr int WPL = 4 / MT;
+template <int MT, int WPL, bool BF16>
+__global__ void __launch_bounds__(stream_max_threads(MT), 1)
+    stream_gemm_kernel(const StreamParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
@@ -94,6 +89,11 @@ __global__ void __launch_bounds__(max_threads<MT>(), 1) stream_gemm_kernel(const
   if (threadIdx.x == 0) {
     for (; issued < min(NS, nchunks); ++issued) issue(issued);
   }
+  // The weights are in flight. Let the next kernel start launching, then
+  // wait for the previous one before touching x or y (both may be its
+  // operands). Without programmatic launch both calls are no-ops.
+  griddep_launch_dependents();
+  griddep_wait();
 
   // This lane's columns and its activations (kept in registers).
   const int k0 = warp * SLICE + lane * EPL;
@@ -173,10 +173,10 @@ __global__ void __launch_bounds__(max_threads<MT>(), 1) stream_gemm_kernel(const
   }
 }
 
-template <int MT, bool BF16>
+template <int MT, int WPL, bool BF16>
 cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int smem_optin,
-                        cudaStream_t stream) {
-  constexpr int SLICE = 32 * 8 * (4 / MT);
+                        bool overlap, cudaStream_t stream) {
+  constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
   const int threads = nw * 32;
   StreamParams p = base;
@@ -191,7 +191,7 @@ cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int sme
     return cudaErrorInvalidConfiguration;
   p.nstages = ns;
   const size_t smem = fixed + static_cast<size_t>(ns) * stage;
-  auto kern = stream_gemm_kernel<MT, BF16>;
+  auto kern = stream_gemm_kernel<MT, WPL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -200,24 +200,27 @@ cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int sme
   if (e != cudaSuccess) return e;
   occ = std::max(occ, 1);
   const int grid = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk, nsm * occ);
-  kern<<<grid, threads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
 
-int max_k_stream(int mt) {
-  const int slice = 32 * 8 * (4 / mt);
-  const int warps = (mt == 1 ? 1024 : 512) / 32;
-  return slice * warps;
-}
+int max_k_stream(int mt) { return mt == 1 ? 32 * 256 * 4 : 32 * 256; }
 
 int stream_tile(int rem, int K) {
-  // up to 4 tokens per pass, fewer when K needs more warps than the
-  // register budget of the wider tile allows
+  // up to 4 tokens per pass; beyond K = 8192 one token per pass
   int mt = rem >= 3 ? 4 : rem;
-  if (mt == 4 && K > max_k_stream(4)) mt = 2;
-  if (mt == 2 && K > max_k_stream(2)) mt = 1;
+  if (mt > 1 && K > max_k_stream(mt)) mt = 1;
   return mt;
 }
 
@@ -229,7 +232,7 @@ int stream_gemm_passes(int M, int K) {
 
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
                                const float *sc, int M, int N, int K, float *y, int ldy,
-                               cudaStream_t stream) {
+                               bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   StreamParams base{};
   base.qw = qw;
@@ -250,15 +253,20 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
     p.y = y + static_cast<size_t>(m0) * ldy;
     p.mt = valid;
     cudaError_t e;
-    if (mt == 1)
-      e = x_bf16 ? launch_pass<1, true>(p, N, K, di.num_sms, di.smem_optin, stream)
-                 : launch_pass<1, false>(p, N, K, di.num_sms, di.smem_optin, stream);
+    // lanes own one packed word per row (8 columns) when K allows, which
+    // gives up to 32 warps per CTA to hide latency; 4 words beyond 8192
+    if (mt == 1 && K <= 8192)
+      e = x_bf16 ? launch_pass<1, 1, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass<1, 1, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
+    else if (mt == 1)
+      e = x_bf16 ? launch_pass<1, 4, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass<1, 4, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     else if (mt == 2)
-      e = x_bf16 ? launch_pass<2, true>(p, N, K, di.num_sms, di.smem_optin, stream)
-                 : launch_pass<2, false>(p, N, K, di.num_sms, di.smem_optin, stream);
+      e = x_bf16 ? launch_pass<2, 1, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass<2, 1, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     else
-      e = x_bf16 ? launch_pass<4, true>(p, N, K, di.num_sms, di.smem_optin, stream)
-                 : launch_pass<4, false>(p, N, K, di.num_sms, di.smem_optin, stream);
+      e = x_bf16 ? launch_pass<4, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass<4, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     if (e != cudaSuccess) return e;
     m0 += valid;
   }

@@ -1,13 +1,421 @@
-// Large-M W4A16 GEMM on tcgen05 tensor cores (bf16 activations).
+// Large-M W4A16 GEMM on the 5th-generation (tcgen05) tensor cores, bf16
+// activations, fp32 accumulation in tensor memory.
+//
+//   y[m][n] = sum_k x[m][k] * W_hat[n][k],  W_hat = (nibble - 8) * scale
+//
+// The contraction is computed transposed, D[n][m] = W_hat_tile * x_tile^T,
+// so that the dequantised weights are the MMA's A operand (M = 128 weight
+// rows per instruction) and the activations its B operand (N = 256 token
+// rows). One CTA owns a 256 (weights) x 256 (tokens) output tile: two
+// 128-row A sub-tiles share every B tile, each with its own 256-column fp32
+// accumulator, filling all 512 TMEM columns.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: 2-D tiled loads of x (128-byte swizzle) into
+//               the B slot of each pipeline stage;
+//   warp 1      TMEM owner and MMA issuer: one elected thread issues
+//               tcgen05.mma (kind::f16, bf16 x bf16 -> f32) per 16-wide K
+//               step and commits each stage back to its producers;
+//   warps 2-9   dequantisers: thread r owns weight row r of the tile, loads
+//               its packed words and scales straight from global memory,
+//               forms fp32 (nibble - 8) * scale exactly, rounds to bf16 and
+//               stores the 16-byte chunks in the canonical K-major 128-byte
+//               swizzled layout the MMA reads; after a tile's last stage
+//               the same warps drain the accumulators (tcgen05.ld) to y.
+// Stage = 64 K columns: A 2 x 16 KB (dequantised) + B 32 KB (TMA); 3 stages.
+// Every wait is bounded; a timeout is recorded in the status word and the
+// CTA unwinds (TMEM is always freed).
+//
+// Format: "The Quiet Commit: How a Single Documentation Edit Marks the
+// Completion of a Major Engineering Milestone", section "The INT4 Milestone".
+// The pages' kernel ran on CUDA cores for sm_120; tensor cores are used here
+// because at large M the product is a dense contraction.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
 #include "kernels.h"
 
 namespace w4a16 {
 
-bool tc_gemm_supported(int, int, int) { return false; }
+namespace {
 
-cudaError_t launch_tc_gemm(const uint16_t *, const int32_t *, const float *, int, int, int,
-                           float *, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int TC_BN = 256;  // weight rows per CTA tile (two MMA A sub-tiles)
+constexpr int TC_BM = 256;  // token rows per CTA tile (MMA N)
+constexpr int TC_BK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int TC_STAGES = 3;
+constexpr int A_SUB_BYTES = 128 * TC_BK * 2;        // 16 KB
+constexpr int A_BYTES = 2 * A_SUB_BYTES;            // 32 KB
+constexpr int B_BYTES = TC_BM * TC_BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 64 KB
+constexpr int TMEM_COLS = 512;
+constexpr int DQ_WARPS = 8;
+constexpr int TC_THREADS = 64 + DQ_WARPS * 32;      // 320
+constexpr int TC_SMEM = TC_STAGES * STAGE_BYTES + 1024 + 256;
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits 7-9
+// = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(TC_BM >> 3) << 17) |
+                            (static_cast<uint32_t>(128 >> 4) << 24);
+
+struct TcParams {
+  const int32_t *qw;
+  const float *sc;
+  float *y;
+  int M, N, K;
+  int tiles_m, num_tiles;
+  int *status;
+};
+
+// Shared-memory matrix descriptor for a K-major operand in the canonical
+// 128-byte swizzled layout: 8-row x 128-byte atoms stacked at 1024-byte
+// stride (SBO), start address in 16-byte units, descriptor version 1,
+// swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;                 // LBO (unused for this layout)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;         // SBO
+  d |= static_cast<uint64_t>(1) << 46;                 // version
+  d |= static_cast<uint64_t>(2) << 61;                 // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 8 packed nibbles (columns 0..7 of the word) * scale -> 8 bf16 in a uint4.
+// (nibble - 8) is formed exactly as an fp32 (magic-number trick, see the
+// streaming kernel), multiplied by the fp32 scale (one rounding, the
+// format's own product), then rounded once more to bf16.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
+  const uint32_t hi = w >> 16;
+  float v[8];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float bias = c == 0 ? 8388616.0f : c == 1 ? 8388736.0f : c == 2 ? 8390656.0f : 8421376.0f;
+    const float sc = c == 0 ? s : c == 1 ? s * 0.0625f : c == 2 ? s * 0.00390625f : s * 0.000244140625f;
+    v[c] = (__uint_as_float((w & (0xFu << (4 * c))) | 0x4B000000u) - bias) * sc;
+    v[4 + c] = (__uint_as_float((hi & (0xFu << (4 * c))) | 0x4B000000u) - bias) * sc;
+  }
+  uint4 o;
+  o.x = pack_bf16x2(v[0], v[1]);
+  o.y = pack_bf16x2(v[2], v[3]);
+  o.z = pack_bf16x2(v[4], v[5]);
+  o.w = pack_bf16x2(v[6], v[7]);
+  return o;
+}
+
+__device__ __forceinline__ bool aborted(const int *flag) {
+  return *reinterpret_cast<const volatile int *>(flag) != 0;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * STAGE_BYTES);
+  uint64_t *empty = full + TC_STAGES;
+  uint64_t *acc_full = empty + TC_STAGES;
+  uint64_t *acc_empty = acc_full + 1;
+  uint64_t *drain = acc_empty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K;
+  const int nk = (K + TC_BK - 1) / TC_BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(&full[s], 1 + DQ_WARPS);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, DQ_WARPS);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    record_status(p.status, W4A16_ERR_TIMEOUT);
+    *reinterpret_cast<volatile int *>(abort_flag) = 1;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
+           tile += gridDim.x) {
+        const int m0 = (tile % p.tiles_m) * TC_BM;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % TC_STAGES;
+          const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
+          if (aborted(abort_flag)) break;
+          mbar_arrive_expect_tx(&full[s], B_BYTES);
+          tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmap_x, kb * TC_BK, m0, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
+           tile += gridDim.x, ++tcount) {
+        if (tcount > 0 && !mbar_wait(acc_empty, static_cast<uint32_t>(tcount - 1) & 1u)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % TC_STAGES;
+          const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k)
+              tc_mma(tmem + sub * TC_BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
+                     sw128_desc(b0 + k * 32), (kb > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+          issued_any = true;
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      // all MMAs this thread issued are complete before TMEM is released
+      if (issued_any) {
+        tc_commit(drain);
+        mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- dequant + epilogue
+    const int dq = threadIdx.x - 64;  // weight row within the tile, 0..255
+    const int sub = dq >> 7, rr = dq & 127;
+    const int Kw = K >> 3;            // packed words per row
+    const int G = K >> 5;
+    // this row's byte offset inside an A sub-tile (swizzle applied per chunk)
+    const uint32_t row_off = static_cast<uint32_t>(sub * A_SUB_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
+    const int swz = rr & 7;
+    const int q = warp & 3;                  // TMEM lane quadrant of this warp
+    const int esub = (warp - 2) >> 2;        // accumulator this warp drains
+    int it = 0, tcount = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
+         tile += gridDim.x, ++tcount) {
+      const int n0 = (tile / p.tiles_m) * TC_BN;
+      const int m0 = (tile % p.tiles_m) * TC_BM;
+      const int n = n0 + dq;
+      const bool nvalid = n < p.N;
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(p.qw + static_cast<size_t>(n) * Kw);
+      const float *srow = p.sc + static_cast<size_t>(n) * G;
+
+      uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
+      float sa = 0.f, sb = 0.f;
+      auto fetch = [&](int kb) {
+        wa = make_uint4(0, 0, 0, 0);
+        wb = make_uint4(0, 0, 0, 0);
+        sa = 0.f;
+        sb = 0.f;
+        if (!nvalid) return;
+        const int w0 = kb * 8;  // first word of this stage
+        if (w0 < Kw) {
+          wa = __ldg(qrow + (w0 >> 2));
+          sa = __ldg(srow + (w0 >> 2));
+        }
+        if (w0 + 4 < Kw) {
+          wb = __ldg(qrow + (w0 >> 2) + 1);
+          sb = __ldg(srow + (w0 >> 2) + 1);
+        }
+      };
+      fetch(0);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % TC_STAGES;
+        const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
+        const uint4 ca = wa, cb = wb;
+        const float csa = sa, csb = sb;
+        if (kb + 1 < nk) fetch(kb + 1);
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
+        if (!got) { fail(); ok = false; break; }
+        uint8_t *arow = smem + s * STAGE_BYTES + row_off;
+        const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = dequant_word(words[c], c < 4 ? csa : csb);
+          *reinterpret_cast<uint4 *>(arow + ((c ^ swz) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+      if (!ok) break;
+      // -------- epilogue: accumulator esub, TMEM lanes q*32 .. q*32+31
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full, static_cast<uint32_t>(tcount) & 1u))) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const int ne = n0 + esub * 128 + q * 32 + lane;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + esub * TC_BM;
+#pragma unroll 1
+      for (int cc = 0; cc < TC_BM / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32cols(tbase + cc * 32, r);
+        const int mb = m0 + cc * 32;
+        if (ne < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (mb + j < p.M) p.y[static_cast<size_t>(mb + j) * p.N + ne] = __uint_as_float(r[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool tc_gemm_supported(int M, int N, int K) {
+  return M > 0 && N > 0 && K > 0 && K % 32 == 0;
+}
+
+cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
+                           int K, float *y, cudaStream_t stream) {
+  const DeviceInfo &di = device_info();
+  auto encode = encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {TC_BK, TC_BM};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.qw = qw;
+  p.sc = sc;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + TC_BM - 1) / TC_BM;
+  const int tiles_n = (N + TC_BN - 1) / TC_BN;
+  p.num_tiles = p.tiles_m * tiles_n;
+  p.status = di.status;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    TC_SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int grid = std::min(p.num_tiles, di.num_sms);
+  tc_gemm_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(tmap, p);
+  return cudaGetLastError();
 }
 
 }  // namespace w4a16

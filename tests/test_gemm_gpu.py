@@ -145,3 +145,85 @@ def test_gemm_on_side_stream(w4):
         y = w4.w4a16_gemm(x, qw, sc, stream=s)
     s.synchronize()
     assert torch.equal(y, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 256, 64), (1, 256, 96), (300, 300, 7168), (257, 513, 160), (64, 4096, 7168),
+    (512, 1000, 2048), (31, 40, 4128),
+])
+def test_tensor_core_path(w4, M, N, K):
+    """The tcgen05 kernel on one-tile, ragged (M, N not multiples of 256;
+    K % 64 == 32) and multi-tile shapes."""
+    run_case(w4, M, N, K, "bf16", seed=M + N + K, algo="tc")
+
+
+def test_tensor_core_path_rejects_fp32(w4):
+    x = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((8, 8), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((8, 2), dtype=torch.float32, device="cuda")
+    with pytest.raises(w4.W4A16Error) as ei:
+        w4.w4a16_gemm(x, qw, sc, algo="tc")
+    assert ei.value.code == w4.W4A16_ERR_UNSUPPORTED
+
+
+def test_tensor_core_deterministic(w4):
+    M, N, K = 700, 900, 1024
+    x = torch.from_numpy(synth.activations(8, M, K)).to(torch.bfloat16).cuda()
+    qw, sc = w4.w4a16_quantize(torch.from_numpy(synth.weights(8, N, K)).cuda())
+    a = w4.w4a16_gemm(x, qw, sc, algo="tc")
+    b = w4.w4a16_gemm(x, qw, sc, algo="tc")
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_overlap_flag_keeps_the_chain_ordered(w4, dt):
+    """With W4A16_FLAG_OVERLAP a call may start streaming weights while the
+    previous kernel runs, but must read x only after it. Chain four GEMMs,
+    each consuming the previous output, into buffers poisoned with NaN: the
+    overlapped chain must give the same bits as the plain one (a read of x
+    before the previous call finished would see NaN or stale values). The
+    first link is also checked against the oracle."""
+    K = 2048
+    x = synth.activations(12, 1, K)
+    ws = [synth.weights(12, K, K, sub=i) for i in range(4)]
+    dev = [w4.w4a16_quantize(torch.from_numpy(w).cuda()) for w in ws]
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+
+    def chain(overlap):
+        bufs = [torch.full((1, K), float("nan"), device="cuda") for _ in dev]
+        ins = [torch.full((1, K), float("nan"), device="cuda", dtype=dtype) for _ in dev]
+        torch.cuda.synchronize()
+        ins[0].copy_(torch.from_numpy(x).to(dtype))
+        for i, (qw, sc) in enumerate(dev):
+            w4.w4a16_gemm(ins[i], qw, sc, y=bufs[i], overlap=overlap)
+            if i + 1 < len(dev):
+                ins[i + 1].copy_(bufs[i].to(dtype))
+        torch.cuda.synchronize()
+        return bufs
+
+    plain = chain(False)
+    over = chain(True)
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    for a, b in zip(plain, over):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.isfinite(a).all()
+    xo = torch.from_numpy(x).to(dtype).float().numpy()
+    q0, c0 = oracle.quantize_w4a16(ws[0])
+    ref, bound = oracle.gemm_ref(xo, q0, c0)
+    assert np.all(np.abs(plain[0].cpu().numpy().astype(np.float64) - ref) <= TOL[dt] * bound)
+
+
+def test_overlap_back_to_back_same_output(w4):
+    """Back-to-back overlapped calls writing the same y (a write-after-write
+    chain) leave the last call's result."""
+    M, N, K = 1, 4096, 7168
+    x = torch.from_numpy(synth.activations(13, M, K)).cuda()
+    qa, sa = w4.w4a16_quantize(torch.from_numpy(synth.weights(13, N, K, sub=0)).cuda())
+    qb, sb = w4.w4a16_quantize(torch.from_numpy(synth.weights(13, N, K, sub=1)).cuda())
+    ref_b = w4.w4a16_gemm(x, qb, sb)
+    y = torch.empty((M, N), device="cuda")
+    for _ in range(5):
+        w4.w4a16_gemm(x, qa, sa, y=y, overlap=True)
+        w4.w4a16_gemm(x, qb, sb, y=y, overlap=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), ref_b.view(torch.int32))
