@@ -174,6 +174,36 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt,
                             void *workspace, size_t ws_bytes,
                             float *y, w4a16_stream_t stream);
 
+/*
+ * w4a16_moe_gemm_noalloc - w4a16_moe_gemm for callers that cannot allocate.
+ * The pages have no counterpart to this entry point; it exists for host
+ * code that may not allocate device memory once it is running (serving
+ * processes that reserve their whole budget at start-up, plugins whose
+ * host framework owns every allocation and offers no workspace, code where
+ * a cudaMalloc would synchronise the device or take the allocator's lock).
+ * It computes exactly what w4a16_moe_gemm computes, with the same
+ * arguments minus the workspace, and calls no allocating routine.
+ *   - Its intermediates live in one fixed device array inside the library:
+ *     40 MiB (41943040 bytes), held by every GPU that loads the library
+ *     until the process exits. Sizes whose w4a16_moe_workspace_size()
+ *     exceeds it are rejected with W4A16_ERR_UNSUPPORTED before any work.
+ *     (128 tokens x top-8, hidden 7168, expert width 2048 need ~37.4 MB.)
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on that device.
+ *   - Every call shares the one array and leaves its contents behind; no
+ *     intermediate needs to start at zero. Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: order them.
+ * Errors: as w4a16_moe_gemm, plus UNSUPPORTED for sizes beyond the array.
+ */
+w4a16_status w4a16_moe_gemm_noalloc(const void *x, w4a16_act_dtype xdt,
+                                    const int32_t *expert_ids, const float *route_w,
+                                    int T, int topk,
+                                    const int32_t *qw_gu, const float *sc_gu,
+                                    const int32_t *qw_dn, const float *sc_dn,
+                                    int E, int H, int I, int group,
+                                    float *y, w4a16_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *w4a16_status_string(w4a16_status s);
 

@@ -48,6 +48,8 @@ SIGNATURES = {
     "w4a16_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "w4a16_moe_gemm": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
                             _VP, _SZ, _VP, _VP]),
+    "w4a16_moe_gemm_noalloc": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I,
+                                    _I, _VP, _VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
     "w4a16_last_device_status": (_I, [_VP]),
 }
@@ -210,6 +212,28 @@ def w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, workspace
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _ptr(y), _stream_handle(stream))
     _check("w4a16_moe_gemm", code)
+    return y
+
+
+def w4a16_moe_gemm_noalloc(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y=None,
+                           group: int = 32, stream=None):
+    """w4a16_moe_gemm without a workspace: the library's fixed 40 MiB device
+    array holds the intermediates (for callers that cannot allocate)."""
+    import torch
+    xdt = _act_dtype(x)
+    _need(x, x.dtype, "x")
+    _need(expert_ids, torch.int32, "expert_ids")
+    _need(route_w, torch.float32, "route_w")
+    T, H = x.shape
+    topk = expert_ids.shape[1]
+    E = qw_gu.shape[0]
+    I = qw_gu.shape[1] // 2
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    code = lib.w4a16_moe_gemm_noalloc(_ptr(x), xdt, _ptr(expert_ids), _ptr(route_w), T, topk,
+                                      _ptr(qw_gu), _ptr(sc_gu), _ptr(qw_dn), _ptr(sc_dn), E, H, I,
+                                      group, _ptr(y), _stream_handle(stream))
+    _check("w4a16_moe_gemm_noalloc", code)
     return y
 
 
