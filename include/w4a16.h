@@ -204,6 +204,14 @@ w4a16_status w4a16_moe_gemm_noalloc(const void *x, w4a16_act_dtype xdt,
                                     int E, int H, int I, int group,
                                     float *y, w4a16_stream_t stream);
 
+/* Testing aid for failure detection: when `enable` is non-zero, the next
+ * launch of the streaming kernel on any device skips issuing its weight
+ * copies, so its waits for them run out (after about one second) and it
+ * records W4A16_ERR_TIMEOUT and returns. The switch clears itself after
+ * that launch. No fault, trap or hang is involved; the context stays
+ * usable. Not for production use. */
+void w4a16_debug_fault_next_launch(int enable);
+
 /* Human-readable name of a status code (static string). */
 const char *w4a16_status_string(w4a16_status s);
 

@@ -50,6 +50,7 @@ SIGNATURES = {
                             _VP, _SZ, _VP, _VP]),
     "w4a16_moe_gemm_noalloc": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I,
                                     _I, _VP, _VP]),
+    "w4a16_debug_fault_next_launch": (None, [_I]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
     "w4a16_last_device_status": (_I, [_VP]),
 }
@@ -235,6 +236,12 @@ def w4a16_moe_gemm_noalloc(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y
                                       group, _ptr(y), _stream_handle(stream))
     _check("w4a16_moe_gemm_noalloc", code)
     return y
+
+
+def w4a16_debug_fault_next_launch(enable: bool = True) -> None:
+    """Testing aid: the next streaming-kernel launch skips its weight copies,
+    times out after about a second and records W4A16_ERR_TIMEOUT."""
+    lib.w4a16_debug_fault_next_launch(1 if enable else 0)
 
 
 def w4a16_last_device_status(stream=None) -> int:

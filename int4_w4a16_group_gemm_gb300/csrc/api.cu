@@ -2,6 +2,7 @@
 // the per-device status word. Declarations and contracts: include/w4a16.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -40,6 +41,12 @@ const DeviceInfo &device_info() {
   std::call_once(g_once[dev], init_device, dev);
   return g_info[dev];
 }
+
+namespace {
+std::atomic<int> g_fault_next{0};
+}
+
+bool take_injected_fault() { return g_fault_next.exchange(0) != 0; }
 
 static bool device_ready() {
   int dev = 0;
@@ -164,6 +171,8 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *e
                               sc_gu, qw_dn, sc_dn, E, H, I, workspace, y,
                               reinterpret_cast<cudaStream_t>(stream)));
 }
+
+void w4a16_debug_fault_next_launch(int enable) { w4a16::g_fault_next.store(enable ? 1 : 0); }
 
 const char *w4a16_status_string(w4a16_status s) {
   switch (s) {

@@ -20,6 +20,10 @@ struct DeviceInfo {
 // Per-device facts, looked up once per device (thread-safe).
 const DeviceInfo &device_info();
 
+// Testing aid: true once after w4a16_debug_fault_next_launch(1); the
+// streaming kernel launched then skips its weight copies.
+bool take_injected_fault();
+
 // ------------------------------------------------------------ streaming kernel
 // y[m0 .. m0+M) = x[m0 .. m0+M) * W_hat^T on CUDA cores, streaming the packed
 // weights once per pass of up to 4 tokens. Any M >= 1; K % 32 == 0,

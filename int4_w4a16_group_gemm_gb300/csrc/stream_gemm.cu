@@ -34,6 +34,7 @@ struct StreamParams {
   int ldy;
   int nstages;
   int sc_bulk;  // 1: scales staged by bulk copy (K % 128 == 0)
+  int fault;    // testing aid: skip the weight copies (waits then time out)
   int *status;
 };
 
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1)
       bulk_g2s(dst + qstage, reinterpret_cast<const uint8_t *>(p.sc) + static_cast<size_t>(row) * srow,
                bs, &full[slot]);
   };
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !p.fault) {
     for (; issued < min(NS, nchunks); ++issued) issue(issued);
   }
   // The weights are in flight. Let the next kernel start launching, then
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1)
     }
     named_bar_sync(1, blockDim.x);
     const bool abort = s_abort != 0;
-    if (threadIdx.x == 0 && !abort && issued < nchunks) {
+    if (threadIdx.x == 0 && !abort && !p.fault && issued < nchunks) {
       issue(issued);
       ++issued;
     }
@@ -243,6 +244,7 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
   base.ldy = ldy;
   base.sc_bulk = (K % 128 == 0) ? 1 : 0;
   base.status = di.status;
+  base.fault = take_injected_fault() ? 1 : 0;
   const size_t xb = x_bf16 ? 2 : 4;
   for (int m0 = 0; m0 < M;) {
     const int rem = M - m0;
