@@ -80,7 +80,8 @@ typedef enum {
  *   group must be 32; K must be a positive multiple of 32; M, N > 0.
  * fp32 mode keeps every output within 1e-5 * sum_k |x*W_hat| of the exact
  * product; bf16 mode within 4e-3 of it (exact product of the bf16 values).
- * Errors: INVALID_ARG, UNSUPPORTED (group != 32, K > 32768), ALIGNMENT, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED (group != 32; K > 16384 on the CUDA-core
+ * path, i.e. fp32 activations or small M), ALIGNMENT, CUDA.
  */
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt,
                         const int32_t *qw, const float *sc,
@@ -163,7 +164,7 @@ size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I);
  *   workspace: device memory of at least w4a16_moe_workspace_size() bytes,
  *   16-byte aligned, owned by the caller; contents on entry are ignored.
  *   y [T][H] fp32 output (overwritten).
- * group must be 32; H and I multiples of 32.
+ * group must be 32; H and I multiples of 32, at most 16384.
  */
 w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt,
                             const int32_t *expert_ids, const float *route_w,

@@ -88,8 +88,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
       if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+      __nanosleep(64);
+    }
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }

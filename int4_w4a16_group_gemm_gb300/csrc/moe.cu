@@ -19,6 +19,7 @@
 //  4. combine:  y[t] = o[t*topk + 0] + o[t*topk + 1] + ... (slot order).
 // Each expert's weights are read once per call whatever its token count.
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.h"
 #include "stream_core.cuh"
@@ -119,16 +120,24 @@ struct MoeParams {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// MODE 0: gate/up + SwiGLU (K = H, 4 gate rows + 4 up rows per stage).
-// MODE 1: down + routing weight (K = I, 8 rows per stage).
+// MODE 0: gate/up + SwiGLU (K = H; a stage holds 4 gate rows and the 4
+//         matching up rows, giving 4 columns of h).
+// MODE 1: down + routing weight (K = I; 8 rows of the down projection).
+// A CTA owns expert blockIdx.y and a range of its stages; the expert's
+// tokens are taken in tiles of MT, one pass over the CTA's rows per tile
+// (most experts have a single tile; later passes find the weights in L2).
+// Within a pass the structure is the dense streaming kernel's: bulk copies
+// into a ring of stages, 8 rows per stage, and the last warp to finish a
+// stage refills it and reduces the warps' partial sums in a fixed order.
 template <int MT, int WPL, bool BF16, int MODE>
-__global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(const MoeParams p) {
+__global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_kernel(const MoeParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
   constexpr int RL = MODE == 0 ? 4 : 8;  // logical output rows per stage
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ int s_issued;
 
   const int e = blockIdx.y;
   const int s0 = p.offsets[e];
@@ -142,6 +151,8 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(c
   const int c_end = static_cast<int>((static_cast<long long>(nlc) * (blockIdx.x + 1)) / gridDim.x);
   const int nchunks = c_end - c_begin;
   if (nchunks <= 0) return;
+  const int ntiles = (ce + MT - 1) / MT;
+  const int total = nchunks * ntiles;  // stages over all passes
 
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,14 +168,8 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(c
 
   uint8_t *stages = smem;
   float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
-  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * nw * RC * MT);
-
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
+  int *count = reinterpret_cast<int *>(red + 2 * NS * nw * RC * MT);
+  uint64_t *full = reinterpret_cast<uint64_t *>(count + ((2 * NS + 1) & ~1));
 
   // global row of stage row r for logical chunk starting at l0 (-1: none)
   auto stage_row = [&](int l0, int r) -> int {
@@ -178,10 +183,9 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(c
     }
   };
 
-  int issued = 0;
-  auto issue = [&](int c) {
-    const int slot = c % NS;
-    const int l0 = (c_begin + c) * RL;
+  auto issue = [&](int gc) {  // gc: stage index over all passes
+    const int slot = gc % NS;
+    const int l0 = (c_begin + gc % nchunks) * RL;
     const int rows = min(RL, L - l0);
     uint8_t *dst = stages + slot * stage_bytes;
     const int parts = MODE == 0 ? 2 : 1;
@@ -193,15 +197,24 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(c
       if (p.sc_bulk) bulk_g2s(dst + qstage + h * 4 * srow, sbase + grow * srow, bs, &full[slot]);
     }
   };
-  if (threadIdx.x == 0)
-    for (; issued < min(NS, nchunks); ++issued) issue(issued);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < 2 * NS; ++i) count[i] = 0;
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    const int first = min(NS, total);
+    for (int gc = 0; gc < first; ++gc) issue(gc);
+    s_issued = first;
+  }
+  __syncthreads();
 
   const int k0 = warp * SLICE + lane * EPL;
   const bool active = k0 < K;
-  const int g = k0 >> 5;
-  const int ntiles = (ce + MT - 1) / MT;
+  const int kc = active ? k0 : 0;
+  const int g = kc >> 5;
 
-  float xr[MT][EPL];
+  uint64_t xr[MT][EPL / 2];
   auto load_tile = [&](int tile) {
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
@@ -225,94 +238,108 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1) moe_stream_kernel(c
       load_x_slice<EPL, BF16>(row, k0, xr[t]);
     }
   };
-  if (ntiles == 1) load_tile(0);
 
-  int it = 0;  // reduction-buffer parity across chunks and tiles
-  int c = 0;
-  for (; c < nchunks; ++c) {
-    const int slot = c % NS;
+  for (int gc = 0; gc < total; ++gc) {
+    const int tile = gc / nchunks;
+    const int c = gc % nchunks;
+    if (c == 0) load_tile(tile);
+    const int slot = gc % NS;
+    const int half = (gc / NS) & 1;
     const int l0 = (c_begin + c) * RL;
-    const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>(c / NS) & 1u);
-    if (!ok) {
-      record_status(p.status, W4A16_ERR_TIMEOUT);
-      s_abort = 1;
+    int ok = 1;
+    if (lane == 0) {
+      ok = (s_abort == 0) && mbar_wait(&full[slot], static_cast<uint32_t>(gc / NS) & 1u);
+      if (!ok && s_abort == 0) {
+        record_status(p.status, W4A16_ERR_TIMEOUT);
+        s_abort = 1;
+      }
     }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) break;
     const uint8_t *st = stages + slot * stage_bytes;
-    bool abort = false;
-    for (int tile = 0; tile < ntiles; ++tile, ++it) {
-      if (ntiles > 1) load_tile(tile);
-      float part[RC][MT];
+    const uint8_t *wbase = st + (kc >> 1);
+    uint32_t wd[RC][WPL];
+    float sv[RC];
 #pragma unroll
-      for (int r = 0; r < RC; ++r) {
-        const int grow = stage_row(l0, r);
-        float acc[MT];
-        if (ok && active && grow >= 0) {
-          uint32_t wd[WPL];
-          load_words<WPL>(st + r * qrow + (k0 >> 1), wd);
-          const float s = p.sc_bulk
-                              ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
-                              : __ldg(reinterpret_cast<const float *>(sbase) +
-                                      static_cast<size_t>(grow) * G + g);
-          lane_dot<MT, WPL>(wd, xr, acc);
+    for (int r = 0; r < RC; ++r) {
+      load_words<WPL>(wbase + r * qrow, wd[r]);
+      const int grow = stage_row(l0, r);
+      sv[r] = p.sc_bulk ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
+                        : (grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
+                                             static_cast<size_t>(grow) * G + g)
+                                     : 0.f);
+    }
+    float part[RC][MT];
+    rows_dot<MT, WPL>(wd, sv, xr, part);
+    float res[MT];
+    warp_reduce_8rows<MT>(part, res, lane);
+    float *redc = red + (static_cast<size_t>(half * NS + slot) * nw) * RC * MT;
+    if ((lane & 3) == 0) {
+      const int row = (lane >> 2) & 7;
 #pragma unroll
-          for (int t = 0; t < MT; ++t) part[r][t] = acc[t] * s;
-        } else {
-#pragma unroll
-          for (int t = 0; t < MT; ++t) part[r][t] = 0.f;
-        }
-      }
-      float res[MT];
-      warp_reduce_8rows<MT>(part, res, lane);
-      float *redb = red + (it & 1) * nw * RC * MT;
-      if ((lane & 3) == 0) {
-        const int row = (lane >> 2) & 7;
-#pragma unroll
-        for (int t = 0; t < MT; ++t) redb[(warp * RC + row) * MT + t] = res[t];
-      }
-      named_bar_sync(1, blockDim.x);
-      abort = s_abort != 0;
-      if (abort) break;
-      if (MODE == 0) {
-        if (threadIdx.x < 4 * MT) {
-          const int jj = threadIdx.x / MT, t = threadIdx.x % MT;
-          const int q = tile * MT + t;
-          if (l0 + jj < p.I && q < ce) {
-            float gs = redb[jj * MT + t], us = redb[(4 + jj) * MT + t];
-            for (int w = 1; w < nw; ++w) {
-              gs += redb[(w * RC + jj) * MT + t];
-              us += redb[(w * RC + 4 + jj) * MT + t];
-            }
-            const float h = silu_f(gs) * us;
-            const size_t idx = static_cast<size_t>(s0 + q) * p.I + l0 + jj;
-            if (BF16)
-              static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
-            else
-              static_cast<float *>(p.out)[idx] = h;
-          }
-        }
-      } else {
-        if (threadIdx.x < RC * MT) {
-          const int row = threadIdx.x / MT, t = threadIdx.x % MT;
-          const int q = tile * MT + t;
-          if (l0 + row < p.H && q < ce) {
-            float v = redb[row * MT + t];
-            for (int w = 1; w < nw; ++w) v += redb[(w * RC + row) * MT + t];
-            const int pair = p.perm[s0 + q];
-            static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + row] =
-                p.route_w[pair] * v;
-          }
-        }
+      for (int t = 0; t < MT; ++t) redc[(warp * RC + row) * MT + t] = res[t];
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&count[half * NS + slot], 1) == nw - 1;
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) continue;
+    // every warp has finished reading this stage: refill it first
+    if (lane == 0) {
+      __threadfence_block();
+      count[half * NS + slot] = 0;
+      if (gc + NS < total && s_abort == 0) {
+        issue(gc + NS);
+        atomicAdd(&s_issued, 1);
       }
     }
-    if (abort) break;
-    // every thread passed the last barrier of this chunk: the slot is free
-    if (threadIdx.x == 0 && issued < nchunks) {
-      issue(issued);
-      ++issued;
+    __syncwarp();
+    // fixed-order sum over the warps: lane (row r, part q) adds warps
+    // q, q+4, ... in order, then the four parts pairwise
+    const int r = lane >> 2, q = lane & 3;
+    float v[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float a = 0.f;
+      for (int w = q; w < nw; w += 4) a += redc[(w * RC + r) * MT + t];
+      a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+      a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+      v[t] = a;
+    }
+    if (MODE == 0) {
+      // lanes of rows 0-3 hold the gate sums, rows 4-7 the up sums
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const float up = __shfl_down_sync(0xFFFFFFFFu, v[t], 16);
+        const int tq = tile * MT + t;
+        if (q == 0 && r < 4 && l0 + r < p.I && tq < ce) {
+          const float h = silu_f(v[t]) * up;
+          const size_t idx = static_cast<size_t>(s0 + tq) * p.I + l0 + r;
+          if (BF16)
+            static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
+          else
+            static_cast<float *>(p.out)[idx] = h;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int tq = tile * MT + t;
+        if (q == 0 && l0 + r < p.H && tq < ce) {
+          const int pair = p.perm[s0 + tq];
+          static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + r] =
+              p.route_w[pair] * v[t];
+        }
+      }
     }
   }
-  if (threadIdx.x == 0 && c < nchunks) {
-    for (int d = c; d < issued; ++d) mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort != 0) {
+    for (int d = max(0, s_issued - NS); d < s_issued; ++d)
+      mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
   }
 }
 
@@ -364,18 +391,26 @@ cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
   constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
   const int threads = nw * 32;
-  const uint32_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
-  const size_t fixed = 2ull * nw * kRowsPerChunk * MT * sizeof(float) + 64;
+  const size_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
   const size_t budget = static_cast<size_t>(di.smem_optin) - 1024;
-  int ns = 4;
-  while (ns > 1 && fixed + static_cast<size_t>(ns) * stage > budget) --ns;
-  if (fixed + static_cast<size_t>(ns) * stage > budget) return cudaErrorInvalidConfiguration;
+  auto bytes_for = [&](int ns) {
+    return static_cast<size_t>(ns) * stage + 2ull * ns * nw * kRowsPerChunk * MT * sizeof(float) +
+           (2 * ns + 2) * sizeof(int) + ns * sizeof(uint64_t) + 64;
+  };
+  // three stages keep two CTAs per SM resident for the widest experts
+  int ns = 3;
+  while (ns > 1 && bytes_for(ns) > budget) --ns;
+  if (bytes_for(ns) > budget) return cudaErrorInvalidConfiguration;
   p.nstages = ns;
-  const size_t smem = fixed + static_cast<size_t>(ns) * stage;
+  const size_t smem = bytes_for(ns);
   auto kern = moe_stream_kernel<MT, WPL, BF16, MODE>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(budget));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   // split every expert into several CTAs so the active experts spread
   // evenly over the SMs (empty experts exit at once)
   const int per_expert = 8;
@@ -388,9 +423,11 @@ template <int MODE>
 cudaError_t launch_expert(MoeParams p, bool bf16, int K, int E, const DeviceInfo &di,
                           cudaStream_t stream) {
   p.sc_bulk = (K % 128 == 0) ? 1 : 0;
-  if (K <= max_k_stream(4))
-    return bf16 ? launch_expert_pass<4, 2, true, MODE>(p, K, E, di, stream)
-                : launch_expert_pass<4, 2, false, MODE>(p, K, E, di, stream);
+  // token tiles of 3 (bf16) or 2 (fp32, whose wider activation registers
+  // would not fit 3) with two packed words per lane up to K = 8192
+  if (K <= max_k_stream(3))
+    return bf16 ? launch_expert_pass<3, 2, true, MODE>(p, K, E, di, stream)
+                : launch_expert_pass<2, 2, false, MODE>(p, K, E, di, stream);
   return bf16 ? launch_expert_pass<1, 4, true, MODE>(p, K, E, di, stream)
               : launch_expert_pass<1, 4, false, MODE>(p, K, E, di, stream);
 }

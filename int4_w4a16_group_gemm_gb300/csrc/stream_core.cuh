@@ -25,9 +25,10 @@ namespace w4a16 {
 
 constexpr int kRowsPerChunk = 8;
 
-// Thread budget of a streaming CTA for a token tile of MT: 1024 threads (64
-// registers each) for MT <= 2, 512 (128 registers) for MT = 4.
-__host__ __device__ constexpr int stream_max_threads(int MT) { return MT == 4 ? 512 : 1024; }
+// Thread budget of a streaming CTA: at most 16 warps, so each thread may
+// use 128 registers (8 rows of packed accumulators per token tile plus the
+// lane's activations).
+__host__ __device__ constexpr int stream_max_threads(int, int = 0) { return 512; }
 
 __device__ __forceinline__ float nib_bias(int c) {
   // 2^23 + 8 * 16^c, exact in fp32 for c = 0..3
@@ -38,21 +39,58 @@ __device__ __forceinline__ float nib_prescale(int c) {
   return c == 0 ? 1.0f : c == 1 ? 0.0625f : c == 2 ? 0.00390625f : 0.000244140625f;
 }
 
-// Load this lane's EPL activations of token row `xrow` (nullptr -> zeros)
-// into xr[], pre-scaled by the nibble-class factor of each column.
+// Packed fp32 pairs: Blackwell's add/fma.f32x2 do two independent fp32
+// operations (each rounded exactly like the scalar one) per instruction.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Load this lane's EPL activations of token row `xrow` (nullptr -> zeros),
+// pre-scaled by the nibble-class factor of each column, as pairs: pair
+// 4*i + c of word i holds columns 8i + c and 8i + 4 + c (the two nibbles of
+// class c in the word's low and high half).
+// Raw activation loads, split from their conversion so that a kernel can
+// issue them early and consume them later. fp32: EPL/4 float4; bf16: EPL/8
+// uint4 (the uint4 array is sized for the fp32 case).
 template <int EPL, bool BF16>
-__device__ __forceinline__ void load_x_slice(const void *xrow, int k0, float (&xr)[EPL]) {
+__device__ __forceinline__ void load_x_raw(const void *xrow, int k0, uint4 (&raw)[EPL / 4]) {
+  constexpr int NV = BF16 ? EPL / 8 : EPL / 4;
   if (xrow == nullptr) {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) xr[i] = 0.f;
+    for (int v = 0; v < EPL / 4; ++v) raw[v] = make_uint4(0, 0, 0, 0);
     return;
   }
+  const uint4 *src = BF16 ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(xrow) + k0)
+                          : reinterpret_cast<const uint4 *>(static_cast<const float *>(xrow) + k0);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) raw[v] = __ldg(src + v);
+}
+
+// Convert raw activations to the pre-scaled pairs lane_dot consumes: pair
+// 4*i + c of word i holds columns 8i + c and 8i + 4 + c (the two nibbles of
+// class c in the word's low and high half), times 16^-c.
+template <int EPL, bool BF16>
+__device__ __forceinline__ void convert_x(const uint4 (&raw)[EPL / 4], uint64_t (&xp)[EPL / 2]) {
+  float xr[EPL];
   if constexpr (BF16) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(xrow) + k0);
 #pragma unroll
     for (int v = 0; v < EPL / 8; ++v) {
-      const uint4 u = __ldg(src + v);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         xr[v * 8 + 2 * h] = __uint_as_float(w[h] << 16);
@@ -60,42 +98,104 @@ __device__ __forceinline__ void load_x_slice(const void *xrow, int k0, float (&x
       }
     }
   } else {
-    const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(xrow) + k0);
 #pragma unroll
     for (int v = 0; v < EPL / 4; ++v) {
-      const float4 f = __ldg(src + v);
-      xr[v * 4 + 0] = f.x;
-      xr[v * 4 + 1] = f.y;
-      xr[v * 4 + 2] = f.z;
-      xr[v * 4 + 3] = f.w;
+      xr[v * 4 + 0] = __uint_as_float(raw[v].x);
+      xr[v * 4 + 1] = __uint_as_float(raw[v].y);
+      xr[v * 4 + 2] = __uint_as_float(raw[v].z);
+      xr[v * 4 + 3] = __uint_as_float(raw[v].w);
     }
   }
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) xr[i] *= nib_prescale((i & 7) & 3);
+  for (int i = 0; i < EPL / 8; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      xp[4 * i + c] = pack_f32x2(xr[8 * i + c] * nib_prescale(c), xr[8 * i + 4 + c] * nib_prescale(c));
+}
+
+// Load this lane's EPL activations of token row `xrow` (nullptr -> zeros)
+// as pre-scaled pairs (see convert_x).
+template <int EPL, bool BF16>
+__device__ __forceinline__ void load_x_slice(const void *xrow, int k0, uint64_t (&xp)[EPL / 2]) {
+  uint4 raw[EPL / 4];
+  load_x_raw<EPL, BF16>(xrow, k0, raw);
+  convert_x<EPL, BF16>(raw, xp);
 }
 
 // acc[t] = sum over this lane's EPL columns of (nibble - 8) * x[t], for the
 // WPL words in `wd` (word i holds columns 8i .. 8i+7 of the lane's slice).
+// Per nibble pair: two LOP3 build 2^23 + n*16^c, one add.f32x2 removes the
+// bias exactly, one fma.f32x2 accumulates; the low-half and high-half
+// chains are added once at the end.
 template <int MT, int WPL>
 __device__ __forceinline__ void lane_dot(const uint32_t (&wd)[WPL],
-                                         const float (&xr)[MT][8 * WPL], float (&acc)[MT]) {
+                                         const uint64_t (&xp)[MT][4 * WPL], float (&acc)[MT]) {
+  uint64_t a[MT];
 #pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+  for (int t = 0; t < MT; ++t) a[t] = 0ull;  // (+0.0f, +0.0f)
 #pragma unroll
   for (int i = 0; i < WPL; ++i) {
     const uint32_t lo = wd[i];
     const uint32_t hi = wd[i] >> 16;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float qlo = __uint_as_float((lo & (0xFu << (4 * c))) | 0x4B000000u) - nib_bias(c);
-      const float qhi = __uint_as_float((hi & (0xFu << (4 * c))) | 0x4B000000u) - nib_bias(c);
+      const float nb = -nib_bias(c);
+      const uint64_t q = add_f32x2(
+          pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | 0x4B000000u),
+                     __uint_as_float((hi & (0xFu << (4 * c))) | 0x4B000000u)),
+          pack_f32x2(nb, nb));
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        acc[t] = fmaf(qlo, xr[t][8 * i + c], acc[t]);
-        acc[t] = fmaf(qhi, xr[t][8 * i + 4 + c], acc[t]);
+      for (int t = 0; t < MT; ++t) a[t] = fma_f32x2(q, xp[t][4 * i + c], a[t]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    float l, h;
+    unpack_f32x2(a[t], l, h);
+    acc[t] = l + h;
+  }
+}
+
+// part[r][t] = scale[r] * sum over this lane's columns of (nibble - 8) * x[t]
+// for the 8 rows of a stage, with the rows interleaved: for every word and
+// nibble class the 8 rows' updates are independent, so 8 FMA chains per
+// token are in flight at once.
+template <int MT, int WPL>
+__device__ __forceinline__ void rows_dot(const uint32_t (&wd)[kRowsPerChunk][WPL],
+                                         const float (&sv)[kRowsPerChunk],
+                                         const uint64_t (&xp)[MT][4 * WPL],
+                                         float (&part)[kRowsPerChunk][MT]) {
+  uint64_t a[kRowsPerChunk][MT];
+#pragma unroll
+  for (int r = 0; r < kRowsPerChunk; ++r)
+#pragma unroll
+    for (int t = 0; t < MT; ++t) a[r][t] = 0ull;
+#pragma unroll
+  for (int i = 0; i < WPL; ++i) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float nb = -nib_bias(c);
+      const uint64_t bias = pack_f32x2(nb, nb);
+#pragma unroll
+      for (int r = 0; r < kRowsPerChunk; ++r) {
+        const uint32_t lo = wd[r][i];
+        const uint64_t q = add_f32x2(
+            pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | 0x4B000000u),
+                       __uint_as_float(((lo >> 16) & (0xFu << (4 * c))) | 0x4B000000u)),
+            bias);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) a[r][t] = fma_f32x2(q, xp[t][4 * i + c], a[r][t]);
       }
     }
   }
+#pragma unroll
+  for (int r = 0; r < kRowsPerChunk; ++r)
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float l, h;
+      unpack_f32x2(a[r][t], l, h);
+      part[r][t] = (l + h) * sv[r];
+    }
 }
 
 // Reduce part[r][t] (8 rows) over the 32 lanes of the warp, in a fixed

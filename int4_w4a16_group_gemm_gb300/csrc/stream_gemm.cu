@@ -15,6 +15,8 @@
 // Accumulation in fp32: "The Silence of Success: A Single Line That Speaks
 // Volumes", section "Assumptions Embedded in the Code".
 #include <algorithm>
+#include <cstdlib>
+#include <mutex>
 
 #include "kernels.h"
 #include "stream_core.cuh"
@@ -38,14 +40,15 @@ struct StreamParams {
   int *status;
 };
 
-template <int MT, int WPL, bool BF16>
-__global__ void __launch_bounds__(stream_max_threads(MT), 1)
+template <int MT, int WPL, bool BF16, bool SCB>
+__global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1)
     stream_gemm_kernel(const StreamParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ int s_issued;
 
   const int K = p.K;
   const int nw = blockDim.x >> 5;
@@ -54,44 +57,49 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1)
   const uint32_t qrow = static_cast<uint32_t>(K) >> 1;  // bytes per packed row
   const uint32_t srow = static_cast<uint32_t>(K) >> 3;  // bytes per scale row
   const uint32_t qstage = RC * qrow;
-  const uint32_t stage_bytes = qstage + (p.sc_bulk ? RC * srow : 0u);
+  const uint32_t stage_bytes = qstage + (SCB ? RC * srow : 0u);
   const int NS = p.nstages;
 
+  // shared memory: NS stages | red[2][NS][nw][RC][MT] | count[2][NS] | full[NS]
   uint8_t *stages = smem;
   float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
-  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * nw * RC * MT);
+  int *count = reinterpret_cast<int *>(red + 2 * NS * nw * RC * MT);
+  uint64_t *full = reinterpret_cast<uint64_t *>(count + ((2 * NS + 1) & ~1));
 
   const int r0 = static_cast<int>((static_cast<long long>(p.N) * blockIdx.x) / gridDim.x);
   const int r1 = static_cast<int>((static_cast<long long>(p.N) * (blockIdx.x + 1)) / gridDim.x);
   const int nchunks = (r1 - r0 + RC - 1) / RC;
 
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  int issued = 0;  // meaningful in thread 0 only
   auto issue = [&](int c) {
     const int slot = c % NS;
     const int row = r0 + c * RC;
     const int rows = min(RC, r1 - row);
     uint8_t *dst = stages + slot * stage_bytes;
     const uint32_t bq = rows * qrow;
-    const uint32_t bs = p.sc_bulk ? rows * srow : 0u;
+    const uint32_t bs = SCB ? rows * srow : 0u;
     mbar_arrive_expect_tx(&full[slot], bq + bs);
     bulk_g2s(dst, reinterpret_cast<const uint8_t *>(p.qw) + static_cast<size_t>(row) * qrow, bq,
              &full[slot]);
-    if (p.sc_bulk)
+    if (SCB)
       bulk_g2s(dst + qstage, reinterpret_cast<const uint8_t *>(p.sc) + static_cast<size_t>(row) * srow,
                bs, &full[slot]);
   };
-  if (threadIdx.x == 0 && !p.fault) {
-    for (; issued < min(NS, nchunks); ++issued) issue(issued);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < 2 * NS; ++i) count[i] = 0;
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    // only the first stage before the activations: the SM serves its
+    // requests roughly in order, and activations queued behind every
+    // stage would arrive last
+    const int first = p.fault ? 0 : min(1, nchunks);
+    for (int c = 0; c < first; ++c) issue(c);
+    s_issued = first;
   }
-  // The weights are in flight. Let the next kernel start launching, then
-  // wait for the previous one before touching x or y (both may be its
+  __syncthreads();
+  // The first weights are in flight. Let the next kernel start launching,
+  // then wait for the previous one before touching x or y (both may be its
   // operands). Without programmatic launch both calls are no-ops.
   griddep_launch_dependents();
   griddep_wait();
@@ -99,8 +107,9 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1)
   // This lane's columns and its activations (kept in registers).
   const int k0 = warp * SLICE + lane * EPL;
   const bool active = k0 < K;
-  const int g = k0 >> 5;
-  float xr[MT][EPL];
+  const int kc = active ? k0 : 0;  // inactive lanes read valid smem, weigh zero
+  const int g = kc >> 5;
+  uint64_t xr[MT][EPL / 2];
 #pragma unroll
   for (int t = 0; t < MT; ++t) {
     const void *xrow = nullptr;
@@ -112,95 +121,158 @@ __global__ void __launch_bounds__(stream_max_threads(MT), 1)
     }
     load_x_slice<EPL, BF16>(xrow, k0, xr[t]);
   }
+  // the activation loads are issued (their registers fill later); now the
+  // remaining stages
+  __syncthreads();
+  if (threadIdx.x == 0 && !p.fault) {
+    const int upto = min(NS, nchunks);
+    for (int c = s_issued; c < upto; ++c) issue(c);
+    s_issued = max(s_issued, upto);
+  }
 
-  int c = 0;
-  for (; c < nchunks; ++c) {
+  for (int c = 0; c < nchunks; ++c) {
     const int slot = c % NS;
-    const uint32_t parity = static_cast<uint32_t>(c / NS) & 1u;
+    const int half = (c / NS) & 1;
     const int row0 = r0 + c * RC;
     const int rows = min(RC, r1 - row0);
-    bool ok = mbar_wait(&full[slot], parity);
-    if (!ok) {
-      record_status(p.status, W4A16_ERR_TIMEOUT);
-      s_abort = 1;
-    }
-    const uint8_t *st = stages + slot * stage_bytes;
-
-    float part[RC][MT];
-#pragma unroll
-    for (int r = 0; r < RC; ++r) {
-      float acc[MT];
-      if (ok && active && r < rows) {
-        uint32_t wd[WPL];
-        load_words<WPL>(st + r * qrow + (k0 >> 1), wd);
-        const float s = p.sc_bulk
-                            ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
-                            : __ldg(p.sc + static_cast<size_t>(row0 + r) * G + g);
-        lane_dot<MT, WPL>(wd, xr, acc);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) part[r][t] = acc[t] * s;
-      } else {
-#pragma unroll
-        for (int t = 0; t < MT; ++t) part[r][t] = 0.f;
+    // lane 0 waits for the stage (sleeping in hardware); __syncwarp then
+    // orders the other lanes' reads after it
+    int ok = 1;
+    if (lane == 0) {
+      ok = (s_abort == 0) && mbar_wait(&full[slot], static_cast<uint32_t>(c / NS) & 1u);
+      if (!ok && s_abort == 0) {
+        record_status(p.status, W4A16_ERR_TIMEOUT);
+        s_abort = 1;
       }
     }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) break;
+    const uint8_t *st = stages + slot * stage_bytes;
+
+    // 8 rows, branch-free: rows past the CTA's range hold stale bytes whose
+    // sums are never stored
+    float part[RC][MT];
+    const uint8_t *wbase = st + (kc >> 1);
+    // all 8 rows' words and scales first, so the loads overlap
+    uint32_t wd[RC][WPL];
+    float sv[RC];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+      load_words<WPL>(wbase + r * qrow, wd[r]);
+      sv[r] = SCB ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
+                  : (r < rows ? __ldg(p.sc + static_cast<size_t>(row0 + r) * G + g) : 0.f);
+    }
+    rows_dot<MT, WPL>(wd, sv, xr, part);
     float res[MT];
     warp_reduce_8rows<MT>(part, res, lane);
-    float *redb = red + (c & 1) * nw * RC * MT;
+    float *redc = red + (static_cast<size_t>(half * NS + slot) * nw) * RC * MT;
     if ((lane & 3) == 0) {
       const int row = (lane >> 2) & 7;
 #pragma unroll
-      for (int t = 0; t < MT; ++t) redb[(warp * RC + row) * MT + t] = res[t];
+      for (int t = 0; t < MT; ++t) redc[(warp * RC + row) * MT + t] = res[t];
     }
-    named_bar_sync(1, blockDim.x);
-    const bool abort = s_abort != 0;
-    if (threadIdx.x == 0 && !abort && !p.fault && issued < nchunks) {
-      issue(issued);
-      ++issued;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&count[half * NS + slot], 1) == nw - 1;
     }
-    if (threadIdx.x < RC * MT && !abort) {
-      const int row = threadIdx.x / MT, t = threadIdx.x % MT;
-      if (row < rows && t < p.mt) {
-        float v = redb[row * MT + t];
-        for (int w = 1; w < nw; ++w) v += redb[(w * RC + row) * MT + t];
-        p.y[static_cast<size_t>(t) * p.ldy + row0 + row] = v;
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last) {
+      // every warp has finished reading this stage: refill it first
+      if (lane == 0) {
+        __threadfence_block();
+        count[half * NS + slot] = 0;
+        if (c + NS < nchunks && s_abort == 0 && !p.fault) {
+          issue(c + NS);
+          atomicAdd(&s_issued, 1);
+        }
+      }
+      __syncwarp();
+      // fixed-order sum over the warps: lane (row r, part q) adds warps
+      // q, q+4, q+8, ... in order, then the four parts pairwise
+      const int r = lane >> 2, q = lane & 3;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        float v = 0.f;
+        for (int w = q; w < nw; w += 4) v += redc[(w * RC + r) * MT + t];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+        if (q == 0 && r < rows && t < p.mt) p.y[static_cast<size_t>(t) * p.ldy + row0 + r] = v;
       }
     }
-    if (abort) break;
   }
   // After an abort, let copies already in flight land before the CTA exits.
-  if (threadIdx.x == 0 && c < nchunks) {
-    for (int d = c; d < issued; ++d) mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort != 0) {
+    for (int d = max(0, s_issued - NS); d < s_issued; ++d)
+      mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
   }
 }
 
-template <int MT, int WPL, bool BF16>
+// Tuning overrides (read once): W4A16_STREAM_NS (stages, 1..8) and
+// W4A16_STREAM_CTAS (CTAs per SM, 1..4); 0 = automatic.
+int env_int(const char *name) {
+  const char *v = getenv(name);
+  return v ? atoi(v) : 0;
+}
+
+template <int MT, int WPL, bool BF16, bool SCB>
 cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int smem_optin,
                         bool overlap, cudaStream_t stream) {
   constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
   const int threads = nw * 32;
   StreamParams p = base;
-  const uint32_t qrow = K / 2, srow = K / 8;
-  const uint32_t stage = kRowsPerChunk * (qrow + (p.sc_bulk ? srow : 0));
-  const size_t fixed = 2ull * nw * kRowsPerChunk * MT * sizeof(float) + 64;
+  const size_t stage = kRowsPerChunk * (K / 2 + (SCB ? K / 8 : 0));
   smem_optin -= 1024;  // room for the kernel's static shared memory
-  const int chunks_per_sm = (N + nsm * kRowsPerChunk - 1) / (nsm * kRowsPerChunk);
-  int ns = std::min(4, std::max(1, chunks_per_sm));
-  while (ns > 1 && fixed + static_cast<size_t>(ns) * stage > static_cast<size_t>(smem_optin)) --ns;
-  if (fixed + static_cast<size_t>(ns) * stage > static_cast<size_t>(smem_optin))
-    return cudaErrorInvalidConfiguration;
+  static const int env_ns = env_int("W4A16_STREAM_NS");
+  static const int env_ctas = env_int("W4A16_STREAM_CTAS");
+  auto bytes_for = [&](int ns) {
+    return static_cast<size_t>(ns) * stage + 2ull * ns * nw * kRowsPerChunk * MT * sizeof(float) +
+           (2 * ns + 2) * sizeof(int) + ns * sizeof(uint64_t) + 64;
+  };
+  // Rows are split evenly over the grid. Each CTA's compute is bound by
+  // instruction latency, so two CTAs per SM (each with up to 3 stages in
+  // flight) stream faster than one with more stages; fall back to one CTA
+  // per SM when two do not fit.
+  int ctas_per_sm = env_ctas > 0 ? std::min(env_ctas, 4) : 2;
+  const int rows_per_cta = (N + nsm * ctas_per_sm - 1) / (nsm * ctas_per_sm);
+  const int want = std::max(1, (rows_per_cta + kRowsPerChunk - 1) / kRowsPerChunk);
+  int ns = env_ns > 0 ? std::min(env_ns, 8) : std::min(ctas_per_sm > 1 ? 3 : 4, want);
+  const size_t per_sm_budget = 227 * 1024;
+  if (env_ctas <= 0 && ctas_per_sm > 1 && ctas_per_sm * (bytes_for(ns) + 1024) > per_sm_budget)
+    ctas_per_sm = 1;
+  while (ns > 1 && bytes_for(ns) > static_cast<size_t>(smem_optin)) --ns;
+  if (bytes_for(ns) > static_cast<size_t>(smem_optin)) return cudaErrorInvalidConfiguration;
   p.nstages = ns;
-  const size_t smem = fixed + static_cast<size_t>(ns) * stage;
-  auto kern = stream_gemm_kernel<MT, WPL, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-  if (e != cudaSuccess) return e;
-  occ = std::max(occ, 1);
-  const int grid = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk, nsm * occ);
+  const size_t smem = bytes_for(ns);
+  auto kern = stream_gemm_kernel<MT, WPL, BF16, SCB>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  // resident CTAs per SM for this configuration (cached for the last one)
+  static std::mutex occ_mu;
+  static size_t occ_smem = 0;
+  static int occ_threads = 0, occ_val = 1;
+  int occ;
+  {
+    std::lock_guard<std::mutex> lk(occ_mu);
+    if (occ_smem != smem || occ_threads != threads) {
+      int o = 0;
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem);
+      if (e != cudaSuccess) return e;
+      occ_smem = smem;
+      occ_threads = threads;
+      occ_val = std::max(o, 1);
+    }
+    occ = occ_val;
+  }
+  const int grid = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk,
+                            nsm * std::min(occ, ctas_per_sm));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
@@ -214,15 +286,22 @@ cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int sme
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int MT, int WPL, bool BF16>
+cudaError_t launch_pass_sc(const StreamParams &p, int N, int K, int nsm, int smem_optin,
+                           bool overlap, cudaStream_t stream) {
+  return p.sc_bulk ? launch_pass<MT, WPL, BF16, true>(p, N, K, nsm, smem_optin, overlap, stream)
+                   : launch_pass<MT, WPL, BF16, false>(p, N, K, nsm, smem_optin, overlap, stream);
+}
+
 }  // namespace
 
-int max_k_stream(int mt) { return mt == 1 ? 32 * 256 * 4 : 32 * 256; }
+int max_k_stream(int mt) { return mt == 1 ? 16384 : 8192; }
 
 int stream_tile(int rem, int K) {
-  // up to 4 tokens per pass; beyond K = 8192 one token per pass
-  int mt = rem >= 3 ? 4 : rem;
-  if (mt > 1 && K > max_k_stream(mt)) mt = 1;
-  return mt;
+  // up to 3 tokens per pass (two packed words per lane, K <= 8192); one
+  // token per pass (four words per lane) up to K = 16384
+  const int mt = rem >= 3 ? 3 : rem;
+  return K > max_k_stream(mt) ? 1 : mt;
 }
 
 int stream_gemm_passes(int M, int K) {
@@ -255,20 +334,20 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
     p.y = y + static_cast<size_t>(m0) * ldy;
     p.mt = valid;
     cudaError_t e;
-    // lanes own one packed word per row (8 columns) when K allows, which
-    // gives up to 32 warps per CTA to hide latency; 4 words beyond 8192
+    // one token: lanes own two packed words per row (16 columns) up to
+    // K = 8192 (16 warps, 128 registers each), four beyond
     if (mt == 1 && K <= 8192)
-      e = x_bf16 ? launch_pass<1, 1, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass<1, 1, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
+      e = x_bf16 ? launch_pass_sc<1, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass_sc<1, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     else if (mt == 1)
-      e = x_bf16 ? launch_pass<1, 4, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass<1, 4, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
+      e = x_bf16 ? launch_pass_sc<1, 4, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass_sc<1, 4, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     else if (mt == 2)
-      e = x_bf16 ? launch_pass<2, 1, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass<2, 1, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
+      e = x_bf16 ? launch_pass_sc<2, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass_sc<2, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     else
-      e = x_bf16 ? launch_pass<4, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass<4, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
+      e = x_bf16 ? launch_pass_sc<3, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
+                 : launch_pass_sc<3, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
     if (e != cudaSuccess) return e;
     m0 += valid;
   }

@@ -97,7 +97,7 @@ def test_prefill_gemm_sampled_rows(w4):
 
 @pytest.mark.parametrize("M,N,K", [
     (1, 1, 32), (2, 13, 96), (3, 1000, 160), (5, 37, 4128), (7, 8, 1024),
-    (4, 100, 8192), (3, 24, 8224), (2, 9, 16384), (1, 5, 32768), (9, 33, 256),
+    (4, 100, 8192), (3, 24, 8224), (2, 9, 16384), (1, 5, 16384), (9, 33, 256),
 ])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_ragged_shapes(w4, M, N, K, dt):
@@ -227,3 +227,13 @@ def test_overlap_back_to_back_same_output(w4):
         w4.w4a16_gemm(x, qb, sb, y=y, overlap=True)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int32), ref_b.view(torch.int32))
+
+
+def test_cuda_core_path_rejects_k_beyond_its_limit(w4):
+    K = 16416
+    x = torch.zeros((1, K), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((4, K // 8), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((4, K // 32), dtype=torch.float32, device="cuda")
+    with pytest.raises(w4.W4A16Error) as ei:
+        w4.w4a16_gemm(x, qw, sc)
+    assert ei.value.code == w4.W4A16_ERR_UNSUPPORTED
