@@ -81,17 +81,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 
 // Wait for phase `parity` of `bar` to complete, giving up after
-// kWaitLimitNs. Returns false on timeout (the caller records it). Waiting
-// threads sleep in hardware between checks, so many waiting warps do not
-// steal issue slots from working ones.
+// kWaitLimitNs. Returns false on timeout (the caller records it). The wait
+// spins: a suspend-time hint or a sleep between checks measurably delays
+// the wake-up on this GPU, and the pipelines here are latency-bound.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 8; ++i) {
-      if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-      __nanosleep(64);
-    }
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }

@@ -124,11 +124,14 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 //         matching up rows, giving 4 columns of h).
 // MODE 1: down + routing weight (K = I; 8 rows of the down projection).
 // A CTA owns expert blockIdx.y and a range of its stages; the expert's
-// tokens are taken in tiles of MT, one pass over the CTA's rows per tile
-// (most experts have a single tile; later passes find the weights in L2).
+// tokens are taken in tiles of MT, and every resident stage serves up to
+// kMoeTiles tiles before it is refilled, so an expert's weights stream from
+// HBM once for up to kMoeTiles * MT tokens (more tokens: further passes).
 // Within a pass the structure is the dense streaming kernel's: bulk copies
 // into a ring of stages, 8 rows per stage, and the last warp to finish a
 // stage refills it and reduces the warps' partial sums in a fixed order.
+constexpr int kMoeTiles = 4;
+
 template <int MT, int WPL, bool BF16, int MODE>
 __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_kernel(const MoeParams p) {
   constexpr int EPL = 8 * WPL;
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
   const int nchunks = c_end - c_begin;
   if (nchunks <= 0) return;
   const int ntiles = (ce + MT - 1) / MT;
-  const int total = nchunks * ntiles;  // stages over all passes
+  const int npass = (ntiles + kMoeTiles - 1) / kMoeTiles;
+  const int total = nchunks * npass;  // stages over all passes
 
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
 
   uint8_t *stages = smem;
   float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
-  int *count = reinterpret_cast<int *>(red + 2 * NS * nw * RC * MT);
+  int *count = reinterpret_cast<int *>(red + 2 * NS * kMoeTiles * nw * RC * MT);
   uint64_t *full = reinterpret_cast<uint64_t *>(count + ((2 * NS + 1) & ~1));
 
   // global row of stage row r for logical chunk starting at l0 (-1: none)
@@ -240,9 +244,11 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
   };
 
   for (int gc = 0; gc < total; ++gc) {
-    const int tile = gc / nchunks;
+    const int pass = gc / nchunks;
     const int c = gc % nchunks;
-    if (c == 0) load_tile(tile);
+    const int t_begin = pass * kMoeTiles;
+    const int nt = min(kMoeTiles, ntiles - t_begin);
+    if (nt == 1 && c == 0) load_tile(t_begin);  // single tile: x stays in registers
     const int slot = gc % NS;
     const int half = (gc / NS) & 1;
     const int l0 = (c_begin + c) * RL;
@@ -258,26 +264,32 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
     if (!ok) break;
     const uint8_t *st = stages + slot * stage_bytes;
     const uint8_t *wbase = st + (kc >> 1);
-    uint32_t wd[RC][WPL];
-    float sv[RC];
+    float *redc = red + (static_cast<size_t>(half * NS + slot) * kMoeTiles) * nw * RC * MT;
+#pragma unroll 1
+    for (int j = 0; j < nt; ++j) {
+      if (nt > 1) load_tile(t_begin + j);
+      // the stage's words and scales, read per tile so that nothing but the
+      // activations stays live across tiles
+      uint32_t wd[RC][WPL];
+      float sv[RC];
 #pragma unroll
-    for (int r = 0; r < RC; ++r) {
-      load_words<WPL>(wbase + r * qrow, wd[r]);
-      const int grow = stage_row(l0, r);
-      sv[r] = p.sc_bulk ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
-                        : (grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
-                                             static_cast<size_t>(grow) * G + g)
-                                     : 0.f);
-    }
-    float part[RC][MT];
-    rows_dot<MT, WPL>(wd, sv, xr, part);
-    float res[MT];
-    warp_reduce_8rows<MT>(part, res, lane);
-    float *redc = red + (static_cast<size_t>(half * NS + slot) * nw) * RC * MT;
-    if ((lane & 3) == 0) {
-      const int row = (lane >> 2) & 7;
+      for (int r = 0; r < RC; ++r) {
+        load_words<WPL>(wbase + r * qrow, wd[r]);
+        const int grow = stage_row(l0, r);
+        sv[r] = p.sc_bulk ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
+                          : (grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
+                                               static_cast<size_t>(grow) * G + g)
+                                       : 0.f);
+      }
+      float part[RC][MT];
+      rows_dot<MT, WPL>(wd, sv, xr, part);
+      float res[MT];
+      warp_reduce_8rows<MT>(part, res, lane);
+      if ((lane & 3) == 0) {
+        const int row = (lane >> 2) & 7;
 #pragma unroll
-      for (int t = 0; t < MT; ++t) redc[(warp * RC + row) * MT + t] = res[t];
+        for (int t = 0; t < MT; ++t) redc[((j * nw + warp) * RC + row) * MT + t] = res[t];
+      }
     }
     __syncwarp();
     int last = 0;
@@ -300,38 +312,41 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
     // fixed-order sum over the warps: lane (row r, part q) adds warps
     // q, q+4, ... in order, then the four parts pairwise
     const int r = lane >> 2, q = lane & 3;
-    float v[MT];
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      float a = 0.f;
-      for (int w = q; w < nw; w += 4) a += redc[(w * RC + r) * MT + t];
-      a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
-      a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
-      v[t] = a;
-    }
-    if (MODE == 0) {
-      // lanes of rows 0-3 hold the gate sums, rows 4-7 the up sums
+    for (int j = 0; j < nt; ++j) {
+      const int tile = t_begin + j;
+      float v[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
-        const float up = __shfl_down_sync(0xFFFFFFFFu, v[t], 16);
-        const int tq = tile * MT + t;
-        if (q == 0 && r < 4 && l0 + r < p.I && tq < ce) {
-          const float h = silu_f(v[t]) * up;
-          const size_t idx = static_cast<size_t>(s0 + tq) * p.I + l0 + r;
-          if (BF16)
-            static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
-          else
-            static_cast<float *>(p.out)[idx] = h;
-        }
+        float a = 0.f;
+        for (int w = q; w < nw; w += 4) a += redc[((j * nw + w) * RC + r) * MT + t];
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+        v[t] = a;
       }
-    } else {
+      if (MODE == 0) {
+        // lanes of rows 0-3 hold the gate sums, rows 4-7 the up sums
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        const int tq = tile * MT + t;
-        if (q == 0 && l0 + r < p.H && tq < ce) {
-          const int pair = p.perm[s0 + tq];
-          static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + r] =
-              p.route_w[pair] * v[t];
+        for (int t = 0; t < MT; ++t) {
+          const float up = __shfl_down_sync(0xFFFFFFFFu, v[t], 16);
+          const int tq = tile * MT + t;
+          if (q == 0 && r < 4 && l0 + r < p.I && tq < ce) {
+            const float h = silu_f(v[t]) * up;
+            const size_t idx = static_cast<size_t>(s0 + tq) * p.I + l0 + r;
+            if (BF16)
+              static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
+            else
+              static_cast<float *>(p.out)[idx] = h;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const int tq = tile * MT + t;
+          if (q == 0 && l0 + r < p.H && tq < ce) {
+            const int pair = p.perm[s0 + tq];
+            static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + r] =
+                p.route_w[pair] * v[t];
+          }
         }
       }
     }
@@ -394,7 +409,8 @@ cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
   const size_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
   const size_t budget = static_cast<size_t>(di.smem_optin) - 1024;
   auto bytes_for = [&](int ns) {
-    return static_cast<size_t>(ns) * stage + 2ull * ns * nw * kRowsPerChunk * MT * sizeof(float) +
+    return static_cast<size_t>(ns) * stage +
+           2ull * ns * kMoeTiles * nw * kRowsPerChunk * MT * sizeof(float) +
            (2 * ns + 2) * sizeof(int) + ns * sizeof(uint64_t) + 64;
   };
   // three stages keep two CTAs per SM resident for the widest experts

@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -43,25 +44,35 @@ namespace w4a16 {
 
 namespace {
 
-constexpr int TC_BN = 256;  // weight rows per CTA tile (two MMA A sub-tiles)
-constexpr int TC_BM = 256;  // token rows per CTA tile (MMA N)
 constexpr int TC_BK = 64;   // K per stage: one 128-byte swizzle row of bf16
-constexpr int TC_STAGES = 3;
 constexpr int A_SUB_BYTES = 128 * TC_BK * 2;        // 16 KB
-constexpr int A_BYTES = 2 * A_SUB_BYTES;            // 32 KB
-constexpr int B_BYTES = TC_BM * TC_BK * 2;          // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 64 KB
-constexpr int TMEM_COLS = 512;
 constexpr int DQ_WARPS = 8;
 constexpr int TC_THREADS = 64 + DQ_WARPS * 32;      // 320
-constexpr int TC_SMEM = TC_STAGES * STAGE_BYTES + 1024 + 256;
 
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits 7-9
-// = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(TC_BM >> 3) << 17) |
-                            (static_cast<uint32_t>(128 >> 4) << 24);
+// Tile shapes. BM is the token width (the MMA N); SUBS the number of
+// 128-row weight sub-tiles per CTA (each an MMA M = 128 with its own TMEM
+// accumulator of BM columns). Large M: BM = 256, SUBS = 2, persistent.
+// M <= 64: BM = 64, SUBS = 1, K split over a cluster.
+template <int BM, int SUBS>
+struct TcCfg {
+  static constexpr int kRows = 128 * SUBS;                 // weight rows per tile
+  static constexpr int kABytes = SUBS * A_SUB_BYTES;
+  static constexpr int kBBytes = BM * TC_BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = SUBS == 2 ? 3 : 8;
+  // stages of packed weights each dequant thread keeps in flight: deep when
+  // every weight comes from HBM (split K), shallow when tiles share them in L2
+  static constexpr int kPrefetch = SUBS == 2 ? 1 : 6;
+  static constexpr int kThreadsPerRow = 256 / kRows;       // dequant threads per row
+  static constexpr int kTmemCols = SUBS * BM < 32 ? 32 : SUBS * BM;  // a power of two
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
+  // 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+  // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     (static_cast<uint32_t>(BM >> 3) << 17) |
+                                     (static_cast<uint32_t>(128 >> 4) << 24);
+};
 
 struct TcParams {
   const int32_t *qw;
@@ -94,12 +105,34 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Distributed shared memory: the address of the same variable in the CTA
+// of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Bulk copy from this CTA's shared memory into a (possibly remote) CTA's
+// shared memory in the cluster, completing on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void *src,
+                                               uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
@@ -166,38 +199,68 @@ __device__ __forceinline__ bool aborted(const int *flag) {
   return *reinterpret_cast<const volatile int *>(flag) != 0;
 }
 
+// SPLIT = false: persistent CTAs walk the (weight-tile, token-tile) grid,
+//   each tile over all of K.
+// SPLIT = true: one tile per cluster; the cluster's CTAs (ranks along grid
+//   y) take consecutive K ranges. Each rank keeps the sum for a slice of
+//   the tile's rows: every CTA parks its fp32 partial tile in shared memory,
+//   pushes each owner's row slice into that owner's shared memory with one
+//   bulk copy, and the owner adds the slices in rank order (deterministic,
+//   no workspace).
+template <int BM, int SUBS, bool SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
+  using Cfg = TcCfg<BM, SUBS>;
+  constexpr int NS = Cfg::kStages;
+  constexpr int SB = Cfg::kStageBytes;
+  constexpr int PD = Cfg::kPrefetch;
+  constexpr int ROWS = Cfg::kRows;
+  constexpr int TPR = Cfg::kThreadsPerRow;
+  constexpr int WPT = 8 / TPR;  // packed words per dequant thread per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * STAGE_BYTES);
-  uint64_t *empty = full + TC_STAGES;
-  uint64_t *acc_full = empty + TC_STAGES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * SB);
+  uint64_t *empty = full + NS;
+  uint64_t *acc_full = empty + NS;
   uint64_t *acc_empty = acc_full + 1;
   uint64_t *drain = acc_empty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *recv_bar = drain + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   const int nk = (K + TC_BK - 1) / TC_BK;
+  const int rank = SPLIT ? static_cast<int>(blockIdx.y) : 0;
+  const int ks = SPLIT ? static_cast<int>(gridDim.y) : 1;
+  // K blocks of this CTA, and its tiles
+  const int kb0 = SPLIT ? static_cast<int>((static_cast<long long>(nk) * rank) / ks) : 0;
+  const int kb1 = SPLIT ? static_cast<int>((static_cast<long long>(nk) * (rank + 1)) / ks) : nk;
+  const int tile_first = blockIdx.x;
+  const int tile_step = SPLIT ? p.num_tiles : gridDim.x;
+  // rows of the tile whose sum rank k keeps
+  auto slice_lo = [&](int k) { return (ROWS * k) / ks; };
+  const int my_rows = slice_lo(rank + 1) - slice_lo(rank);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1 + DQ_WARPS);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, DQ_WARPS);
     mbar_init(drain, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // this rank receives ks slices of my_rows x BM floats
+    if (SPLIT) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(ks * my_rows * BM * 4));
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -215,16 +278,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       int it = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
-           tile += gridDim.x) {
-        const int m0 = (tile % p.tiles_m) * TC_BM;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % TC_STAGES;
-          const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
+      for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag); tile += tile_step) {
+        const int m0 = (tile % p.tiles_m) * BM;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
           if (aborted(abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], B_BYTES);
-          tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmap_x, kb * TC_BK, m0, &full[s]);
+          mbar_arrive_expect_tx(&full[s], Cfg::kBBytes);
+          tma_load_2d(smem + s * SB + Cfg::kABytes, &tmap_x, kb * TC_BK, m0, &full[s]);
         }
       }
     }
@@ -233,27 +295,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       int it = 0, tcount = 0;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
-           tile += gridDim.x, ++tcount) {
+      for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag);
+           tile += tile_step, ++tcount) {
         if (tcount > 0 && !mbar_wait(acc_empty, static_cast<uint32_t>(tcount - 1) & 1u)) {
           fail();
           break;
         }
         tc_fence_after();
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % TC_STAGES;
-          const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t b0 = a0 + A_BYTES;
+          const uint32_t a0 = smem_u32(smem + s * SB);
+          const uint32_t b0 = a0 + Cfg::kABytes;
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub)
+          for (int sub = 0; sub < SUBS; ++sub)
 #pragma unroll
             for (int k = 0; k < TC_BK / 16; ++k)
-              tc_mma(tmem + sub * TC_BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
-                     sw128_desc(b0 + k * 32), (kb > 0 || k > 0) ? 1u : 0u);
+              tc_mma(tmem + sub * BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
+                     sw128_desc(b0 + k * 32), Cfg::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
           issued_any = true;
         }
@@ -268,63 +330,83 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------- dequant + epilogue
-    const int dq = threadIdx.x - 64;  // weight row within the tile, 0..255
-    const int sub = dq >> 7, rr = dq & 127;
-    const int Kw = K >> 3;            // packed words per row
+    const int dq = threadIdx.x - 64;                  // 0..255
+    const int row = dq / TPR, part = dq % TPR;        // weight row within the tile
+    const int sub = row >> 7, rr = row & 127;
+    const int Kw = K >> 3;                            // packed words per row
     const int G = K >> 5;
-    // this row's byte offset inside an A sub-tile (swizzle applied per chunk)
-    const uint32_t row_off = static_cast<uint32_t>(sub * A_SUB_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
+    // this row's byte offset inside the A region (swizzle applied per chunk)
+    const uint32_t row_off =
+        static_cast<uint32_t>(sub * A_SUB_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
     const int swz = rr & 7;
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
     const int esub = (warp - 2) >> 2;        // accumulator this warp drains
     int it = 0, tcount = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles && !aborted(abort_flag);
-         tile += gridDim.x, ++tcount) {
-      const int n0 = (tile / p.tiles_m) * TC_BN;
-      const int m0 = (tile % p.tiles_m) * TC_BM;
-      const int n = n0 + dq;
+    for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag);
+         tile += tile_step, ++tcount) {
+      const int n0 = (tile / p.tiles_m) * ROWS;
+      const int m0 = (tile % p.tiles_m) * BM;
+      const int n = n0 + row;
       const bool nvalid = n < p.N;
       const uint4 *qrow = reinterpret_cast<const uint4 *>(p.qw + static_cast<size_t>(n) * Kw);
       const float *srow = p.sc + static_cast<size_t>(n) * G;
 
-      uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-      float sa = 0.f, sb = 0.f;
-      auto fetch = [&](int kb) {
-        wa = make_uint4(0, 0, 0, 0);
-        wb = make_uint4(0, 0, 0, 0);
-        sa = 0.f;
-        sb = 0.f;
-        if (!nvalid) return;
-        const int w0 = kb * 8;  // first word of this stage
-        if (w0 < Kw) {
-          wa = __ldg(qrow + (w0 >> 2));
-          sa = __ldg(srow + (w0 >> 2));
+      // register ring of PD prefetched stages (slots indexed at compile time);
+      // each stage of this thread: WPT words (one or two uint4) and their scales
+      uint4 ra[PD][WPT / 4];
+      float rs[PD][WPT / 4];
+      auto fetch = [&](int kb, uint4 (&w)[WPT / 4], float (&sc)[WPT / 4]) {
+#pragma unroll
+        for (int h = 0; h < WPT / 4; ++h) {
+          w[h] = make_uint4(0, 0, 0, 0);
+          sc[h] = 0.f;
         }
-        if (w0 + 4 < Kw) {
-          wb = __ldg(qrow + (w0 >> 2) + 1);
-          sb = __ldg(srow + (w0 >> 2) + 1);
+        if (!nvalid || kb >= kb1) return;
+#pragma unroll
+        for (int h = 0; h < WPT / 4; ++h) {
+          const int w0 = kb * 8 + part * WPT + 4 * h;  // first word of this piece
+          if (w0 < Kw) {
+            w[h] = __ldg(qrow + (w0 >> 2));
+            sc[h] = __ldg(srow + (w0 >> 2));
+          }
         }
       };
-      fetch(0);
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % TC_STAGES;
-        const uint32_t ph = static_cast<uint32_t>(it / TC_STAGES) & 1u;
-        const uint4 ca = wa, cb = wb;
-        const float csa = sa, csb = sb;
-        if (kb + 1 < nk) fetch(kb + 1);
-        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
-        if (!got) { fail(); ok = false; break; }
-        uint8_t *arow = smem + s * STAGE_BYTES + row_off;
-        const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = dequant_word(words[c], c < 4 ? csa : csb);
-          *reinterpret_cast<uint4 *>(arow + ((c ^ swz) << 4)) = v;
+      for (int u = 0; u < PD; ++u) fetch(kb0 + u, ra[u], rs[u]);
+      bool ok = true;
+      for (int kbase = kb0; kbase < kb1 && ok; kbase += PD) {
+#pragma unroll
+        for (int u = 0; u < PD; ++u) {
+          const int kb = kbase + u;
+          if (kb >= kb1) break;
+          const int s = it % NS;
+          const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+          ++it;
+          uint4 cw[WPT / 4];
+          float cs[WPT / 4];
+#pragma unroll
+          for (int h = 0; h < WPT / 4; ++h) {
+            cw[h] = ra[u][h];
+            cs[h] = rs[u][h];
+          }
+          fetch(kb + PD, ra[u], rs[u]);
+          const bool got =
+              __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
+          if (!got) { fail(); ok = false; break; }
+          uint8_t *arow = smem + s * SB + row_off;
+#pragma unroll
+          for (int h = 0; h < WPT / 4; ++h) {
+            const uint32_t words[4] = {cw[h].x, cw[h].y, cw[h].z, cw[h].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = part * WPT + 4 * h + c;
+              *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) = dequant_word(words[c], cs[h]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
       }
       if (!ok) break;
       // -------- epilogue: accumulator esub, TMEM lanes q*32 .. q*32+31
@@ -333,18 +415,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int ne = n0 + esub * 128 + q * 32 + lane;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + esub * TC_BM;
+      if (esub < SUBS) {
+        const int nl = esub * 128 + q * 32 + lane;  // row within the tile
+        const int ne = n0 + nl;
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + esub * BM;
+        // split: partial tile to shared memory, row-major with the 16-byte
+        // chunks of each row rotated by the row index (the lanes of a warp,
+        // 32 consecutive rows, then hit different banks); the stages are idle
+        float *red = reinterpret_cast<float *>(smem);
 #pragma unroll 1
-      for (int cc = 0; cc < TC_BM / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld_32cols(tbase + cc * 32, r);
-        const int mb = m0 + cc * 32;
-        if (ne < p.N) {
+        for (int cc = 0; cc < BM / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + cc * 32, r);
+          if (SPLIT) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (mb + j < p.M) p.y[static_cast<size_t>(mb + j) * p.N + ne] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) {
+              const int m = cc * 32 + j;
+              red[nl * BM + ((((m >> 2) ^ nl) & (BM / 4 - 1)) << 2) + (m & 3)] = __uint_as_float(r[j]);
+            }
+          } else {
+            const int mb = m0 + cc * 32;
+            if (ne < p.N) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (mb + j < p.M) p.y[static_cast<size_t>(mb + j) * p.N + ne] = __uint_as_float(r[j]);
+            }
+          }
         }
+        if (SPLIT) fence_proxy_async_smem();  // the bulk copies read `red`
       }
       tc_fence_before();
       __syncwarp();
@@ -352,10 +450,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   __syncthreads();
+  if (SPLIT) {
+    // every CTA of the cluster has parked its partial tile
+    cluster_sync_all();
+    const int n0 = (tile_first / p.tiles_m) * ROWS;
+    const int m0 = (tile_first % p.tiles_m) * BM;
+    const float *red = reinterpret_cast<const float *>(smem);
+    const float *recv = red + ROWS * BM;  // [ks][my_rows][BM]
+    const bool ok_here = *reinterpret_cast<volatile int *>(abort_flag) == 0;
+    if (threadIdx.x == 0) {
+      // push owner k's rows of this partial tile into its receive area
+      for (int k = 0; k < ks; ++k) {
+        const int lo = slice_lo(k), rows_k = slice_lo(k + 1) - lo;
+        const uint32_t dst = cluster_map(smem_u32(recv + rank * rows_k * BM), k);
+        bulk_s2cluster(dst, red + lo * BM, static_cast<uint32_t>(rows_k * BM * 4),
+                       cluster_map(smem_u32(recv_bar), k));
+      }
+    }
+    const bool got = mbar_wait(recv_bar, 0);
+    if (!got) fail();
+    if (got && ok_here) {
+      const int lo = slice_lo(rank);
+      for (int e = threadIdx.x; e < my_rows * BM; e += blockDim.x) {
+        const int i = e % my_rows, m = e / my_rows;  // consecutive threads: consecutive rows
+        const int nl = lo + i;
+        if (n0 + nl >= p.N || m0 + m >= p.M) continue;
+        const int col = ((((m >> 2) ^ nl) & (BM / 4 - 1)) << 2) + (m & 3);
+        float v = recv[i * BM + col];
+        for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * BM + col];
+        p.y[static_cast<size_t>(m0 + m) * p.N + n0 + nl] = v;
+      }
+    }
+    // no CTA leaves while its shared memory may still be copied from
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(TMEM_COLS)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
   }
 }
@@ -380,15 +512,55 @@ bool tc_gemm_supported(int M, int N, int K) {
   return M > 0 && N > 0 && K > 0 && K % 32 == 0;
 }
 
+namespace {
+
+template <int BM, int SUBS, bool SPLIT>
+cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, int ks,
+                      cudaStream_t stream) {
+  using Cfg = TcCfg<BM, SUBS>;
+  auto kern = tc_gemm_kernel<BM, SUBS, SPLIT>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, SPLIT ? ks : 1);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = SPLIT ? ks : 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+}
+
+int env_int(const char *name) {
+  const char *v = getenv(name);
+  return v ? atoi(v) : 0;
+}
+
+}  // namespace
+
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
                            int K, float *y, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
+  // M <= 64: 128 x 64 tiles with K split over a cluster of up to 4 CTAs, so
+  // that every SM streams weights; otherwise 256 x 256 persistent tiles
+  const bool small = M <= 64;
+  const int BM = small ? 64 : 256;
+  const int ROWS = small ? 128 : 256;
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {TC_BK, TC_BM};
+  const cuuint32_t box[2] = {TC_BK, static_cast<cuuint32_t>(BM)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -402,20 +574,18 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_m = (M + TC_BM - 1) / TC_BM;
-  const int tiles_n = (N + TC_BN - 1) / TC_BN;
+  p.tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = (N + ROWS - 1) / ROWS;
   p.num_tiles = p.tiles_m * tiles_n;
   p.status = di.status;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    TC_SMEM);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  const int grid = std::min(p.num_tiles, di.num_sms);
-  tc_gemm_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(tmap, p);
-  return cudaGetLastError();
+  if (small) {
+    static const int env_ks = env_int("W4A16_TC_KS");  // tuning override
+    const int kmax = env_ks > 0 ? std::min(env_ks, 8) : 4;
+    const int nk = (K + TC_BK - 1) / TC_BK;
+    const int ks = std::max(1, std::min(std::min(kmax, nk), di.num_sms / std::max(1, p.num_tiles)));
+    return launch_tc<64, 1, true>(tmap, p, p.num_tiles, ks, stream);
+  }
+  return launch_tc<256, 2, false>(tmap, p, std::min(p.num_tiles, di.num_sms), 1, stream);
 }
 
 }  // namespace w4a16
