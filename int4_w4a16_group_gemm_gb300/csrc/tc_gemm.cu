@@ -46,8 +46,6 @@ namespace {
 
 constexpr int TC_BK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int A_SUB_BYTES = 128 * TC_BK * 2;        // 16 KB
-constexpr int DQ_WARPS = 8;
-constexpr int TC_THREADS = 64 + DQ_WARPS * 32;      // 320
 
 // Tile shapes. BM is the token width (the MMA N); SUBS the number of
 // 128-row weight sub-tiles per CTA (each an MMA M = 128 with its own TMEM
@@ -55,6 +53,8 @@ constexpr int TC_THREADS = 64 + DQ_WARPS * 32;      // 320
 // M <= 64: BM = 64, SUBS = 1, K split over a cluster.
 template <int BM, int SUBS>
 struct TcCfg {
+  static constexpr int kDqWarps = SUBS == 2 ? 8 : 16;      // dequantiser warps
+  static constexpr int kThreads = 64 + 32 * kDqWarps;      // + TMA warp + MMA warp
   static constexpr int kRows = 128 * SUBS;                 // weight rows per tile
   static constexpr int kABytes = SUBS * A_SUB_BYTES;
   static constexpr int kBBytes = BM * TC_BK * 2;
@@ -63,7 +63,7 @@ struct TcCfg {
   // stages of packed weights each dequant thread keeps in flight: deep when
   // every weight comes from HBM (split K), shallow when tiles share them in L2
   static constexpr int kPrefetch = SUBS == 2 ? 1 : 6;
-  static constexpr int kThreadsPerRow = 256 / kRows;       // dequant threads per row
+  static constexpr int kThreadsPerRow = 32 * kDqWarps / kRows;  // dequant threads per row
   static constexpr int kTmemCols = SUBS * BM < 32 ? 32 : SUBS * BM;  // a power of two
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
@@ -208,7 +208,7 @@ __device__ __forceinline__ bool aborted(const int *flag) {
 //   bulk copy, and the owner adds the slices in rank order (deterministic,
 //   no workspace).
 template <int BM, int SUBS, bool SPLIT>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
   using Cfg = TcCfg<BM, SUBS>;
   constexpr int NS = Cfg::kStages;
@@ -217,6 +217,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   constexpr int ROWS = Cfg::kRows;
   constexpr int TPR = Cfg::kThreadsPerRow;
   constexpr int WPT = 8 / TPR;  // packed words per dequant thread per stage
+  constexpr int DQ_WARPS = Cfg::kDqWarps;
+  constexpr int PIECES = WPT >= 4 ? WPT / 4 : 1;  // 16-byte loads per stage
+  constexpr int PW = WPT >= 4 ? 4 : WPT;          // words per load
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------- dequant + epilogue
-    const int dq = threadIdx.x - 64;                  // 0..255
+    const int dq = threadIdx.x - 64;                  // 0 .. 32 * DQ_WARPS - 1
     const int row = dq / TPR, part = dq % TPR;        // weight row within the tile
     const int sub = row >> 7, rr = row & 127;
     const int Kw = K >> 3;                            // packed words per row
@@ -352,21 +355,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const float *srow = p.sc + static_cast<size_t>(n) * G;
 
       // register ring of PD prefetched stages (slots indexed at compile time);
-      // each stage of this thread: WPT words (one or two uint4) and their scales
-      uint4 ra[PD][WPT / 4];
-      float rs[PD][WPT / 4];
-      auto fetch = [&](int kb, uint4 (&w)[WPT / 4], float (&sc)[WPT / 4]) {
+      // each stage of this thread: WPT words and their scale(s)
+      uint32_t ra[PD][WPT];
+      float rs[PD][PIECES];
+      auto fetch = [&](int kb, uint32_t (&w)[WPT], float (&sc)[PIECES]) {
 #pragma unroll
-        for (int h = 0; h < WPT / 4; ++h) {
-          w[h] = make_uint4(0, 0, 0, 0);
-          sc[h] = 0.f;
-        }
+        for (int i = 0; i < WPT; ++i) w[i] = 0u;
+#pragma unroll
+        for (int h = 0; h < PIECES; ++h) sc[h] = 0.f;
         if (!nvalid || kb >= kb1) return;
 #pragma unroll
-        for (int h = 0; h < WPT / 4; ++h) {
-          const int w0 = kb * 8 + part * WPT + 4 * h;  // first word of this piece
+        for (int h = 0; h < PIECES; ++h) {
+          const int w0 = kb * 8 + part * WPT + PW * h;  // first word of this piece
           if (w0 < Kw) {
-            w[h] = __ldg(qrow + (w0 >> 2));
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(qrow) + w0;
+            if (PW == 4) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+              w[4 * h] = v.x; w[4 * h + 1] = v.y; w[4 * h + 2] = v.z; w[4 * h + 3] = v.w;
+            } else if (PW == 2) {
+              const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src));
+              w[0] = v.x; w[1] = v.y;
+            } else {
+              w[0] = __ldg(src);
+            }
             sc[h] = __ldg(srow + (w0 >> 2));
           }
         }
@@ -382,26 +393,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           ++it;
-          uint4 cw[WPT / 4];
-          float cs[WPT / 4];
+          uint32_t cw[WPT];
+          float cs[PIECES];
 #pragma unroll
-          for (int h = 0; h < WPT / 4; ++h) {
-            cw[h] = ra[u][h];
-            cs[h] = rs[u][h];
-          }
+          for (int i = 0; i < WPT; ++i) cw[i] = ra[u][i];
+#pragma unroll
+          for (int h = 0; h < PIECES; ++h) cs[h] = rs[u][h];
           fetch(kb + PD, ra[u], rs[u]);
           const bool got =
               __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
           if (!got) { fail(); ok = false; break; }
           uint8_t *arow = smem + s * SB + row_off;
 #pragma unroll
-          for (int h = 0; h < WPT / 4; ++h) {
-            const uint32_t words[4] = {cw[h].x, cw[h].y, cw[h].z, cw[h].w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int chunk = part * WPT + 4 * h + c;
-              *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) = dequant_word(words[c], cs[h]);
-            }
+          for (int i = 0; i < WPT; ++i) {
+            const int chunk = part * WPT + i;
+            *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) =
+                dequant_word(cw[i], cs[i / PW]);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -527,7 +534,7 @@ cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, in
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_x, SPLIT ? ks : 1);
-  cfg.blockDim = dim3(TC_THREADS);
+  cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
