@@ -94,6 +94,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, but also gives up (returning false) once `*abort` becomes
+// nonzero: another warp of the CTA has already timed out, so the phase may
+// never complete. The flag is polled between batches of try_waits.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   const volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort != 0 || globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ---------------------------------------------------------------- bulk copy
 // 1-D bulk copy global -> shared, completion signalled on `bar` as tx bytes.
 // dst/src 16-byte aligned, bytes a multiple of 16.
@@ -123,6 +137,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------- numbers
+// `v`, returned through a warp shuffle so that the compiler cannot fold it
+// into an instruction immediate. The nibble unpack computes
+// (word & mask) | 0x4B000000: with both constants as immediates that takes
+// two logic instructions, with the pattern in a register one three-input
+// logic instruction, and the logic pipe is the unpack's bottleneck. All 32
+// lanes of the warp must call it together.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
+  return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+
+// Exponent pattern of 2^23: OR-ing an integer m < 2^23 into it gives the
+// fp32 number 2^23 + m.
+constexpr uint32_t kMagic2p23 = 0x4B000000u;
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }

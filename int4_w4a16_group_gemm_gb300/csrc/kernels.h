@@ -25,19 +25,20 @@ const DeviceInfo &device_info();
 bool take_injected_fault();
 
 // ------------------------------------------------------------ streaming kernel
-// y[m0 .. m0+M) = x[m0 .. m0+M) * W_hat^T on CUDA cores, streaming the packed
-// weights once per pass of up to 3 tokens. Any M >= 1; K % 32 == 0,
-// K <= 16384. `ldx`/`ldy` are row strides in elements. `overlap` launches
-// with programmatic stream serialisation: the weight stream may start before
-// the previous kernel on the stream has finished (x and y stay ordered).
+// y = x * W_hat^T on CUDA cores for any M >= 1 (K % 32 == 0, K <= 16384),
+// in one launch: a 2-D grid of row blocks x token tiles of up to 3 tokens.
+// `ldx`/`ldy` are row strides in elements. `overlap` launches with
+// programmatic stream serialisation: the weight stream may start before the
+// previous kernel on the stream has finished (x and y stay ordered).
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
                                const float *sc, int M, int N, int K, float *y, int ldy,
                                bool overlap, cudaStream_t stream);
 // Largest K the streaming kernel accepts for a token tile of `mt` (1, 2, 3).
 int max_k_stream(int mt);
-// Token tile width the streaming kernel uses for `rem` remaining tokens.
-int stream_tile(int rem, int K);
-// Number of streaming-kernel launches for M tokens.
+// Token tile width the streaming kernel uses for M tokens.
+int stream_tile(int M, int K);
+// Number of streaming-kernel launches for M tokens (1 unless the tiles
+// exceed the grid's y limit).
 int stream_gemm_passes(int M, int K);
 
 // ------------------------------------------------------------ tensor-core kernel

@@ -10,10 +10,11 @@
 //
 // Nibble unpacking without integer->float conversion instructions: nibble j
 // of a word sits in bits 4j..4j+3. For the four nibbles of a 16-bit half,
-// (half & (0xF << 4c)) | 0x4B000000 is the fp32 number 2^23 + nibble*16^c,
-// so subtracting 2^23 + 8*16^c gives (nibble - 8) * 16^c exactly. The
-// matching activation is pre-multiplied by 16^-c (an exact power-of-two
-// scaling), so each FMA adds the exact product (nibble - 8) * x.
+// (half & (0xF << 4c)) | 0x4B000000 is the fp32 number 2^23 + nibble*16^c
+// (one logic instruction when the pattern comes in as `magic`, see
+// opaque_u32), so subtracting 2^23 + 8*16^c gives (nibble - 8) * 16^c
+// exactly. The matching activation is pre-multiplied by 16^-c (an exact
+// power-of-two scaling), so each FMA adds the exact product (nibble - 8) * x.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -129,7 +130,8 @@ __device__ __forceinline__ void load_x_slice(const void *xrow, int k0, uint64_t 
 // chains are added once at the end.
 template <int MT, int WPL>
 __device__ __forceinline__ void lane_dot(const uint32_t (&wd)[WPL],
-                                         const uint64_t (&xp)[MT][4 * WPL], float (&acc)[MT]) {
+                                         const uint64_t (&xp)[MT][4 * WPL], float (&acc)[MT],
+                                         uint32_t magic) {
   uint64_t a[MT];
 #pragma unroll
   for (int t = 0; t < MT; ++t) a[t] = 0ull;  // (+0.0f, +0.0f)
@@ -141,8 +143,8 @@ __device__ __forceinline__ void lane_dot(const uint32_t (&wd)[WPL],
     for (int c = 0; c < 4; ++c) {
       const float nb = -nib_bias(c);
       const uint64_t q = add_f32x2(
-          pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | 0x4B000000u),
-                     __uint_as_float((hi & (0xFu << (4 * c))) | 0x4B000000u)),
+          pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | magic),
+                     __uint_as_float((hi & (0xFu << (4 * c))) | magic)),
           pack_f32x2(nb, nb));
 #pragma unroll
       for (int t = 0; t < MT; ++t) a[t] = fma_f32x2(q, xp[t][4 * i + c], a[t]);
@@ -164,7 +166,7 @@ template <int MT, int WPL>
 __device__ __forceinline__ void rows_dot(const uint32_t (&wd)[kRowsPerChunk][WPL],
                                          const float (&sv)[kRowsPerChunk],
                                          const uint64_t (&xp)[MT][4 * WPL],
-                                         float (&part)[kRowsPerChunk][MT]) {
+                                         float (&part)[kRowsPerChunk][MT], uint32_t magic) {
   uint64_t a[kRowsPerChunk][MT];
 #pragma unroll
   for (int r = 0; r < kRowsPerChunk; ++r)
@@ -180,8 +182,8 @@ __device__ __forceinline__ void rows_dot(const uint32_t (&wd)[kRowsPerChunk][WPL
       for (int r = 0; r < kRowsPerChunk; ++r) {
         const uint32_t lo = wd[r][i];
         const uint64_t q = add_f32x2(
-            pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | 0x4B000000u),
-                       __uint_as_float(((lo >> 16) & (0xFu << (4 * c))) | 0x4B000000u)),
+            pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | magic),
+                       __uint_as_float(((lo >> 16) & (0xFu << (4 * c))) | magic)),
             bias);
 #pragma unroll
         for (int t = 0; t < MT; ++t) a[r][t] = fma_f32x2(q, xp[t][4 * i + c], a[r][t]);

@@ -1,13 +1,15 @@
 // Small-M W4A16 GEMM on CUDA cores: the memory-bound decode / tree-verify
 // kernel. y[m][n] = sum_k x[m][k] * (nibble(n,k) - 8) * sc[n][k/32].
 //
-// Each CTA owns a contiguous range of weight rows. Because qw and sc are
-// row-major, that range is one contiguous run of bytes in each tensor, so a
-// single thread streams it into a ring of shared-memory stages with 1-D bulk
-// copies (8 rows per stage, several stages in flight from the first cycle),
-// and every warp consumes the stages (see stream_core.cuh for the split of
+// The grid is row blocks x token tiles. A CTA owns a contiguous range of
+// weight rows and up to 3 tokens. Because qw and sc are row-major, the row
+// range is one contiguous run of bytes in each tensor, so a producer warp
+// streams it into a ring of shared-memory stages with 1-D bulk copies (8
+// rows per stage, the whole ring in flight from the first cycle), and the
+// consumer warps unpack and multiply (see stream_core.cuh for the split of
 // K over warps and lanes). The per-warp row sums are combined across the
-// CTA's warps in a fixed order, so results are deterministic.
+// CTA's warps in a fixed order, so results are deterministic. Token tiles
+// of the same rows re-read the weights, from L2 when they fit there.
 //
 // Format: "The Quiet Commit: How a Single Documentation Edit Marks the
 // Completion of a Major Engineering Milestone", section "The INT4 Milestone"
@@ -28,7 +30,7 @@ namespace {
 struct StreamParams {
   const void *x;
   int ldx;
-  int mt;  // valid tokens in this pass (<= MT)
+  int M;  // tokens; CTA row blockIdx.y covers tokens [MT*blockIdx.y, MT*blockIdx.y + MT)
   const int32_t *qw;
   const float *sc;
   int N, K;
@@ -40,18 +42,29 @@ struct StreamParams {
   int *status;
 };
 
-template <int MT, int WPL, bool BF16, bool SCB>
-__global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1)
-    stream_gemm_kernel(const StreamParams p) {
+// Largest row block of a CTA (bounds the table of per-warp row sums).
+constexpr int kMaxRowsPerCta = 128;
+
+// Roles: warps 0 .. nw-1 consume (each owns one K-slice of every row, see
+// stream_core.cuh) and the last warp produces: it issues the bulk copies
+// into the ring of stages and refills a stage as soon as every consumer has
+// loaded its words from it (the stage's `empty` mbarrier). Consumers never
+// wait for each other. Up to two tokens, each keeps one chunk in flight:
+// the cross-lane reduction of chunk c is issued together with the FMAs of
+// chunk c + 1. The per-warp row sums go to a shared-memory table that holds
+// every row of the CTA. After the last chunk the whole CTA adds the table
+// over the warps in a fixed order and writes y.
+template <int MT, int WPL, bool BF16, bool SCB, int MAXW, int MINB>
+__global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const StreamParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
+  constexpr bool kDeferReduce = MT <= 2;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
-  __shared__ int s_issued;
 
   const int K = p.K;
-  const int nw = blockDim.x >> 5;
+  const int nw = (blockDim.x >> 5) - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = K >> 5;
   const uint32_t qrow = static_cast<uint32_t>(K) >> 1;  // bytes per packed row
@@ -59,16 +72,18 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1)
   const uint32_t qstage = RC * qrow;
   const uint32_t stage_bytes = qstage + (SCB ? RC * srow : 0u);
   const int NS = p.nstages;
-
-  // shared memory: NS stages | red[2][NS][nw][RC][MT] | count[2][NS] | full[NS]
-  uint8_t *stages = smem;
-  float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
-  int *count = reinterpret_cast<int *>(red + 2 * NS * nw * RC * MT);
-  uint64_t *full = reinterpret_cast<uint64_t *>(count + ((2 * NS + 1) & ~1));
+  const int m0 = blockIdx.y * MT;
+  const int mt = min(MT, p.M - m0);
 
   const int r0 = static_cast<int>((static_cast<long long>(p.N) * blockIdx.x) / gridDim.x);
   const int r1 = static_cast<int>((static_cast<long long>(p.N) * (blockIdx.x + 1)) / gridDim.x);
   const int nchunks = (r1 - r0 + RC - 1) / RC;
+
+  // shared memory: NS stages | full[NS] | empty[NS] | red[nchunks*RC][MT][nw]
+  uint8_t *stages = smem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
+  uint64_t *empty = full + NS;
+  float *red = reinterpret_cast<float *>(empty + NS);
 
   auto issue = [&](int c) {
     const int slot = c % NS;
@@ -85,273 +100,290 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1)
                bs, &full[slot]);
   };
 
-  if (threadIdx.x == 0) {
+  // The producer's lane 0 sets up the ring and starts the weight stream at
+  // once: the weights are not written by the previous kernel on the stream
+  // (the overlap contract), so they may be read before it has finished.
+  const int first = p.fault ? 0 : min(NS, nchunks);
+  if (threadIdx.x == nw * 32) {
     s_abort = 0;
-    for (int i = 0; i < 2 * NS; ++i) count[i] = 0;
-    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nw);
+    }
     fence_mbar_init();
-    // only the first stage before the activations: the SM serves its
-    // requests roughly in order, and activations queued behind every
-    // stage would arrive last
-    const int first = p.fault ? 0 : min(1, nchunks);
     for (int c = 0; c < first; ++c) issue(c);
-    s_issued = first;
   }
   __syncthreads();
-  // The first weights are in flight. Let the next kernel start launching,
-  // then wait for the previous one before touching x or y (both may be its
-  // operands). Without programmatic launch both calls are no-ops.
+  // Let the next kernel start launching, then wait for the previous one
+  // before touching x or y (both may be its operands). Without programmatic
+  // launch both calls are no-ops.
   griddep_launch_dependents();
   griddep_wait();
 
-  // This lane's columns and its activations (kept in registers).
-  const int k0 = warp * SLICE + lane * EPL;
-  const bool active = k0 < K;
-  const int kc = active ? k0 : 0;  // inactive lanes read valid smem, weigh zero
-  const int g = kc >> 5;
-  uint64_t xr[MT][EPL / 2];
-#pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    const void *xrow = nullptr;
-    if (active && t < p.mt) {
-      xrow = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
-                                              static_cast<size_t>(t) * p.ldx)
-                  : static_cast<const void *>(static_cast<const float *>(p.x) +
-                                              static_cast<size_t>(t) * p.ldx);
-    }
-    load_x_slice<EPL, BF16>(xrow, k0, xr[t]);
-  }
-  // the activation loads are issued (their registers fill later); now the
-  // remaining stages
-  __syncthreads();
-  if (threadIdx.x == 0 && !p.fault) {
-    const int upto = min(NS, nchunks);
-    for (int c = s_issued; c < upto; ++c) issue(c);
-    s_issued = max(s_issued, upto);
-  }
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int slot = c % NS;
-    const int half = (c / NS) & 1;
-    const int row0 = r0 + c * RC;
-    const int rows = min(RC, r1 - row0);
-    // lane 0 waits for the stage (sleeping in hardware); __syncwarp then
-    // orders the other lanes' reads after it
-    int ok = 1;
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ok = (s_abort == 0) && mbar_wait(&full[slot], static_cast<uint32_t>(c / NS) & 1u);
-      if (!ok && s_abort == 0) {
-        record_status(p.status, W4A16_ERR_TIMEOUT);
-        s_abort = 1;
+      int issued = first, released = 0;
+      for (int c = 0; c + NS < nchunks && !p.fault; ++c) {
+        if (!mbar_wait_or_abort(&empty[c % NS], static_cast<uint32_t>(c / NS) & 1u, &s_abort)) {
+          if (atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
+          break;
+        }
+        released = c + 1;
+        issue(c + NS);
+        ++issued;
       }
+      // After an abort, let the copies still in flight land before the CTA
+      // exits (each wait is bounded; a landed copy completes at once).
+      if (static_cast<volatile int &>(s_abort) != 0)
+        for (int d = released; d < issued; ++d)
+          mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
     }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) break;
-    const uint8_t *st = stages + slot * stage_bytes;
+  } else {
+    // ------------------------------------------------------------ consumers
+    const uint32_t magic = opaque_u32(kMagic2p23);
+    // This lane's columns and its activations (kept in registers).
+    const int k0 = warp * SLICE + lane * EPL;
+    const bool active = k0 < K;
+    const int kc = active ? k0 : 0;  // inactive lanes read valid smem, weigh zero
+    const int g = kc >> 5;
+    uint64_t xr[MT][EPL / 2];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const void *xrow = nullptr;
+      if (active && t < mt) {
+        const size_t off = static_cast<size_t>(m0 + t) * p.ldx;
+        xrow = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) + off)
+                    : static_cast<const void *>(static_cast<const float *>(p.x) + off);
+      }
+      load_x_slice<EPL, BF16>(xrow, k0, xr[t]);
+    }
 
-    // 8 rows, branch-free: rows past the CTA's range hold stale bytes whose
-    // sums are never stored
-    float part[RC][MT];
-    const uint8_t *wbase = st + (kc >> 1);
-    // all 8 rows' words and scales first, so the loads overlap
+    // Wait for chunk c, copy this lane's words and scales of its 8 rows to
+    // registers and release the stage. Rows past the CTA's range hold stale
+    // bytes whose sums are never stored (the reduction keeps rows apart).
+    auto fetch = [&](int c, uint32_t (&wd)[RC][WPL], float (&sv)[RC]) -> bool {
+      const int slot = c % NS;
+      const int row0 = r0 + c * RC;
+      if (!SCB) {
+        const int rows = min(RC, r1 - row0);
+#pragma unroll
+        for (int r = 0; r < RC; ++r)
+          sv[r] = r < rows ? __ldg(p.sc + static_cast<size_t>(row0 + r) * G + g) : 0.f;
+      }
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait_or_abort(&full[slot], static_cast<uint32_t>(c / NS) & 1u, &s_abort);
+        if (!ok && atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+      const uint8_t *st = stages + slot * stage_bytes;
+      const uint8_t *wbase = st + (kc >> 1);
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        load_words<WPL>(wbase + r * qrow, wd[r]);
+        if (SCB) sv[r] = reinterpret_cast<const float *>(st + qstage + r * srow)[g];
+      }
+      // the loads above have returned once their values are used; order
+      // them before the release with a warp barrier
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      return true;
+    };
+    auto store_sums = [&](int c, const float (&part)[RC][MT]) {
+      float res[MT];
+      warp_reduce_8rows<MT>(part, res, lane);
+      if ((lane & 3) == 0) {
+        const int row = c * RC + ((lane >> 2) & 7);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) red[(row * MT + t) * nw + warp] = res[t];
+      }
+    };
+
     uint32_t wd[RC][WPL];
     float sv[RC];
+    if constexpr (kDeferReduce) {
+      float prev[RC][MT];
+      bool ok = nchunks > 0 && fetch(0, wd, sv);
+      if (ok) rows_dot<MT, WPL>(wd, sv, xr, prev, magic);
+      for (int c = 1; ok && c < nchunks; ++c) {
+        ok = fetch(c, wd, sv);
+        if (!ok) break;
+        float part[RC][MT];
+        rows_dot<MT, WPL>(wd, sv, xr, part, magic);
+        store_sums(c - 1, prev);
 #pragma unroll
-    for (int r = 0; r < RC; ++r) {
-      load_words<WPL>(wbase + r * qrow, wd[r]);
-      sv[r] = SCB ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
-                  : (r < rows ? __ldg(p.sc + static_cast<size_t>(row0 + r) * G + g) : 0.f);
-    }
-    rows_dot<MT, WPL>(wd, sv, xr, part);
-    float res[MT];
-    warp_reduce_8rows<MT>(part, res, lane);
-    float *redc = red + (static_cast<size_t>(half * NS + slot) * nw) * RC * MT;
-    if ((lane & 3) == 0) {
-      const int row = (lane >> 2) & 7;
+        for (int r = 0; r < RC; ++r)
 #pragma unroll
-      for (int t = 0; t < MT; ++t) redc[(warp * RC + row) * MT + t] = res[t];
-    }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&count[half * NS + slot], 1) == nw - 1;
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (last) {
-      // every warp has finished reading this stage: refill it first
-      if (lane == 0) {
-        __threadfence_block();
-        count[half * NS + slot] = 0;
-        if (c + NS < nchunks && s_abort == 0 && !p.fault) {
-          issue(c + NS);
-          atomicAdd(&s_issued, 1);
-        }
+          for (int t = 0; t < MT; ++t) prev[r][t] = part[r][t];
       }
-      __syncwarp();
-      // fixed-order sum over the warps: lane (row r, part q) adds warps
-      // q, q+4, q+8, ... in order, then the four parts pairwise
-      const int r = lane >> 2, q = lane & 3;
-#pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        float v = 0.f;
-        for (int w = q; w < nw; w += 4) v += redc[(w * RC + r) * MT + t];
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-        if (q == 0 && r < rows && t < p.mt) p.y[static_cast<size_t>(t) * p.ldy + row0 + r] = v;
+      if (ok && nchunks > 0) store_sums(nchunks - 1, prev);
+    } else {
+      // three tokens: no registers to spare for a chunk in flight
+      for (int c = 0; c < nchunks; ++c) {
+        if (!fetch(c, wd, sv)) break;
+        float part[RC][MT];
+        rows_dot<MT, WPL>(wd, sv, xr, part, magic);
+        store_sums(c, part);
       }
     }
   }
-  // After an abort, let copies already in flight land before the CTA exits.
+
+  // ------------------------------------------------------------ epilogue
+  // Every consumer's sums are in the table: add them over the warps in a
+  // fixed order (warp 0 first) and write y.
   __syncthreads();
-  if (threadIdx.x == 0 && s_abort != 0) {
-    for (int d = max(0, s_issued - NS); d < s_issued; ++d)
-      mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+  if (static_cast<volatile int &>(s_abort) != 0) return;
+  const int nrows = r1 - r0;
+  for (int i = threadIdx.x; i < nrows * MT; i += blockDim.x) {
+    const int row = i / MT, t = i - row * MT;
+    if (t >= mt) continue;
+    const float *v = red + static_cast<size_t>(i) * nw;
+    float a = 0.f;
+    for (int w = 0; w < nw; ++w) a += v[w];
+    p.y[static_cast<size_t>(m0 + t) * p.ldy + r0 + row] = a;
   }
 }
 
-// Tuning overrides (read once): W4A16_STREAM_NS (stages, 1..8) and
-// W4A16_STREAM_CTAS (CTAs per SM, 1..4); 0 = automatic.
+// Tuning overrides (read once): W4A16_STREAM_NS (stages, 1..8),
+// W4A16_STREAM_CTAS (row blocks per SM, 1..4); 0 = automatic.
 int env_int(const char *name) {
   const char *v = getenv(name);
   return v ? atoi(v) : 0;
 }
 
-template <int MT, int WPL, bool BF16, bool SCB>
-cudaError_t launch_pass(const StreamParams &base, int N, int K, int nsm, int smem_optin,
-                        bool overlap, cudaStream_t stream) {
+template <int MT, int WPL, bool BF16, bool SCB, int MAXW, int MINB>
+cudaError_t launch_tiles(const StreamParams &base, int tiles, int N, int K, int nsm,
+                         int smem_optin, bool overlap, cudaStream_t stream) {
   constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
-  const int threads = nw * 32;
+  const int threads = (nw + 1) * 32;
+  if (nw + 1 > MAXW) return cudaErrorInvalidConfiguration;
   StreamParams p = base;
   const size_t stage = kRowsPerChunk * (K / 2 + (SCB ? K / 8 : 0));
-  smem_optin -= 1024;  // room for the kernel's static shared memory
   static const int env_ns = env_int("W4A16_STREAM_NS");
   static const int env_ctas = env_int("W4A16_STREAM_CTAS");
-  auto bytes_for = [&](int ns) {
-    return static_cast<size_t>(ns) * stage + 2ull * ns * nw * kRowsPerChunk * MT * sizeof(float) +
-           (2 * ns + 2) * sizeof(int) + ns * sizeof(uint64_t) + 64;
-  };
-  // Rows are split evenly over the grid. Each CTA's compute is bound by
-  // instruction latency, so two CTAs per SM (each with up to 3 stages in
-  // flight) stream faster than one with more stages; fall back to one CTA
-  // per SM when two do not fit.
-  int ctas_per_sm = env_ctas > 0 ? std::min(env_ctas, 4) : 2;
-  const int rows_per_cta = (N + nsm * ctas_per_sm - 1) / (nsm * ctas_per_sm);
+  // One row block per SM (more when a block would exceed kMaxRowsPerCta
+  // rows). With MINB == 2 the CTA is sized (registers and shared memory) so
+  // that a CTA of the next call on the stream fits beside it: under
+  // programmatic launch that CTA starts its weight stream while this one
+  // computes.
+  const int ctas_per_sm = env_ctas > 0 ? std::min(env_ctas, 4) : 1;
+  int gx = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk, nsm * ctas_per_sm);
+  gx = std::max({1, gx, (N + kMaxRowsPerCta - 1) / kMaxRowsPerCta});
+  const int rows_per_cta = (N + gx - 1) / gx;
   const int want = std::max(1, (rows_per_cta + kRowsPerChunk - 1) / kRowsPerChunk);
-  int ns = env_ns > 0 ? std::min(env_ns, 8) : std::min(ctas_per_sm > 1 ? 3 : 4, want);
-  const size_t per_sm_budget = 227 * 1024;
-  if (env_ctas <= 0 && ctas_per_sm > 1 && ctas_per_sm * (bytes_for(ns) + 1024) > per_sm_budget)
-    ctas_per_sm = 1;
-  while (ns > 1 && bytes_for(ns) > static_cast<size_t>(smem_optin)) --ns;
-  if (bytes_for(ns) > static_cast<size_t>(smem_optin)) return cudaErrorInvalidConfiguration;
+  auto bytes_for = [&](int ns) {
+    return static_cast<size_t>(ns) * stage + 2ull * ns * sizeof(uint64_t) +
+           static_cast<size_t>(want) * kRowsPerChunk * MT * nw * sizeof(float);
+  };
+  const size_t budget = std::min<size_t>(static_cast<size_t>(smem_optin) - 1024,
+                                         MINB >= 2 ? (227u * 1024u) / 2 - 2048 : 227u * 1024u);
+  int ns = env_ns > 0 ? std::min(env_ns, 8) : std::min(want, 4);
+  while (ns > 1 && bytes_for(ns) > budget) --ns;
+  if (bytes_for(ns) > static_cast<size_t>(smem_optin) - 1024) return cudaErrorInvalidConfiguration;
   p.nstages = ns;
   const size_t smem = bytes_for(ns);
-  auto kern = stream_gemm_kernel<MT, WPL, BF16, SCB>;
+  auto kern = stream_gemm_kernel<MT, WPL, BF16, SCB, MAXW, MINB>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_optin - 1024);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  // resident CTAs per SM for this configuration (cached for the last one)
-  static std::mutex occ_mu;
-  static size_t occ_smem = 0;
-  static int occ_threads = 0, occ_val = 1;
-  int occ;
-  {
-    std::lock_guard<std::mutex> lk(occ_mu);
-    if (occ_smem != smem || occ_threads != threads) {
-      int o = 0;
-      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem);
-      if (e != cudaSuccess) return e;
-      occ_smem = smem;
-      occ_threads = threads;
-      occ_val = std::max(o, 1);
-    }
-    occ = occ_val;
-  }
-  const int grid = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk,
-                            nsm * std::min(occ, ctas_per_sm));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  for (int t0 = 0; t0 < tiles; t0 += 65535) {
+    const int nt = std::min(tiles - t0, 65535);
+    StreamParams q = p;
+    q.M = std::min(p.M - t0 * MT, nt * MT);
+    q.x = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
+                                           static_cast<size_t>(t0) * MT * p.ldx)
+               : static_cast<const void *>(static_cast<const float *>(p.x) +
+                                           static_cast<size_t>(t0) * MT * p.ldx);
+    q.y = p.y + static_cast<size_t>(t0) * MT * p.ldy;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, nt);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-template <int MT, int WPL, bool BF16>
-cudaError_t launch_pass_sc(const StreamParams &p, int N, int K, int nsm, int smem_optin,
-                           bool overlap, cudaStream_t stream) {
-  return p.sc_bulk ? launch_pass<MT, WPL, BF16, true>(p, N, K, nsm, smem_optin, overlap, stream)
-                   : launch_pass<MT, WPL, BF16, false>(p, N, K, nsm, smem_optin, overlap, stream);
+template <int MT, int WPL, bool BF16, int MAXW, int MINB>
+cudaError_t launch_tiles_sc(const StreamParams &p, int tiles, int N, int K, int nsm,
+                            int smem_optin, bool overlap, cudaStream_t stream) {
+  return p.sc_bulk
+             ? launch_tiles<MT, WPL, BF16, true, MAXW, MINB>(p, tiles, N, K, nsm, smem_optin,
+                                                             overlap, stream)
+             : launch_tiles<MT, WPL, BF16, false, MAXW, MINB>(p, tiles, N, K, nsm, smem_optin,
+                                                              overlap, stream);
 }
 
 }  // namespace
 
 int max_k_stream(int mt) { return mt == 1 ? 16384 : 8192; }
 
-int stream_tile(int rem, int K) {
-  // up to 3 tokens per pass (two packed words per lane, K <= 8192); one
-  // token per pass (four words per lane) up to K = 16384
-  const int mt = rem >= 3 ? 3 : rem;
-  return K > max_k_stream(mt) ? 1 : mt;
+// Largest K for token tiles of 2 or 3 (15 consumer warps of two packed
+// words per lane, plus the producer: 16 warps keep 128 registers a thread).
+constexpr int kMaxKMultiToken = 15 * 512;
+
+int stream_tile(int M, int K) {
+  // up to 3 tokens per CTA (two packed words per lane); one token per CTA
+  // beyond kMaxKMultiToken (four words per lane up to K = 16384)
+  return K > kMaxKMultiToken ? 1 : std::min(M, 3);
 }
 
 int stream_gemm_passes(int M, int K) {
-  int n = 0;
-  for (int m0 = 0; m0 < M; ++n) m0 += std::min(stream_tile(M - m0, K), M - m0);
-  return n;
+  const int tiles = (M + stream_tile(M, K) - 1) / stream_tile(M, K);
+  return (tiles + 65534) / 65535;
 }
 
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
                                const float *sc, int M, int N, int K, float *y, int ldy,
                                bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
-  StreamParams base{};
-  base.qw = qw;
-  base.sc = sc;
-  base.N = N;
-  base.K = K;
-  base.ldx = ldx;
-  base.ldy = ldy;
-  base.sc_bulk = (K % 128 == 0) ? 1 : 0;
-  base.status = di.status;
-  base.fault = take_injected_fault() ? 1 : 0;
-  const size_t xb = x_bf16 ? 2 : 4;
-  for (int m0 = 0; m0 < M;) {
-    const int rem = M - m0;
-    const int mt = stream_tile(rem, K);
-    const int valid = std::min(mt, rem);
-    StreamParams p = base;
-    p.x = static_cast<const uint8_t *>(x) + static_cast<size_t>(m0) * ldx * xb;
-    p.y = y + static_cast<size_t>(m0) * ldy;
-    p.mt = valid;
-    cudaError_t e;
-    // one token: lanes own two packed words per row (16 columns) up to
-    // K = 8192 (16 warps, 128 registers each), four beyond
-    if (mt == 1 && K <= 8192)
-      e = x_bf16 ? launch_pass_sc<1, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass_sc<1, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
-    else if (mt == 1)
-      e = x_bf16 ? launch_pass_sc<1, 4, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass_sc<1, 4, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
-    else if (mt == 2)
-      e = x_bf16 ? launch_pass_sc<2, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass_sc<2, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
-    else
-      e = x_bf16 ? launch_pass_sc<3, 2, true>(p, N, K, di.num_sms, di.smem_optin, overlap, stream)
-                 : launch_pass_sc<3, 2, false>(p, N, K, di.num_sms, di.smem_optin, overlap, stream);
-    if (e != cudaSuccess) return e;
-    m0 += valid;
-  }
-  return cudaSuccess;
+  StreamParams p{};
+  p.x = x;
+  p.ldx = ldx;
+  p.M = M;
+  p.qw = qw;
+  p.sc = sc;
+  p.N = N;
+  p.K = K;
+  p.y = y;
+  p.ldy = ldy;
+  p.sc_bulk = (K % 128 == 0) ? 1 : 0;
+  p.status = di.status;
+  p.fault = take_injected_fault() ? 1 : 0;
+  const int mt = stream_tile(M, K);
+  const int tiles = (M + mt - 1) / mt;
+  const int nsm = di.num_sms, opt = di.smem_optin;
+  // One token: lanes own two packed words per row (16 columns) up to
+  // K = 7680, four beyond. Up to K = 7168 the CTA (14 consumer warps and the
+  // producer, at most 64 registers a thread) leaves room for a CTA of the
+  // next call.
+  if (mt == 1 && K <= 7168)
+    return x_bf16 ? launch_tiles_sc<1, 2, true, 15, 2>(p, tiles, N, K, nsm, opt, overlap, stream)
+                  : launch_tiles_sc<1, 2, false, 15, 2>(p, tiles, N, K, nsm, opt, overlap, stream);
+  if (mt == 1 && K <= kMaxKMultiToken)
+    return x_bf16 ? launch_tiles_sc<1, 2, true, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream)
+                  : launch_tiles_sc<1, 2, false, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream);
+  if (mt == 1)
+    return x_bf16 ? launch_tiles_sc<1, 4, true, 17, 1>(p, tiles, N, K, nsm, opt, overlap, stream)
+                  : launch_tiles_sc<1, 4, false, 17, 1>(p, tiles, N, K, nsm, opt, overlap, stream);
+  if (mt == 2)
+    return x_bf16 ? launch_tiles_sc<2, 2, true, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream)
+                  : launch_tiles_sc<2, 2, false, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream);
+  return x_bf16 ? launch_tiles_sc<3, 2, true, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream)
+                : launch_tiles_sc<3, 2, false, 16, 1>(p, tiles, N, K, nsm, opt, overlap, stream);
 }
 
 }  // namespace w4a16

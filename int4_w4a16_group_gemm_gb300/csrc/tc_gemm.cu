@@ -177,15 +177,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (nibble - 8) is formed exactly as an fp32 (magic-number trick, see the
 // streaming kernel), multiplied by the fp32 scale (one rounding, the
 // format's own product), then rounded once more to bf16.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, uint32_t magic) {
   const uint32_t hi = w >> 16;
   float v[8];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const float bias = c == 0 ? 8388616.0f : c == 1 ? 8388736.0f : c == 2 ? 8390656.0f : 8421376.0f;
     const float sc = c == 0 ? s : c == 1 ? s * 0.0625f : c == 2 ? s * 0.00390625f : s * 0.000244140625f;
-    v[c] = (__uint_as_float((w & (0xFu << (4 * c))) | 0x4B000000u) - bias) * sc;
-    v[4 + c] = (__uint_as_float((hi & (0xFu << (4 * c))) | 0x4B000000u) - bias) * sc;
+    v[c] = (__uint_as_float((w & (0xFu << (4 * c))) | magic) - bias) * sc;
+    v[4 + c] = (__uint_as_float((hi & (0xFu << (4 * c))) | magic) - bias) * sc;
   }
   uint4 o;
   o.x = pack_bf16x2(v[0], v[1]);
@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------- dequant + epilogue
+    const uint32_t magic = opaque_u32(kMagic2p23);
     const int dq = threadIdx.x - 64;                  // 0 .. 32 * DQ_WARPS - 1
     const int row = dq / TPR, part = dq % TPR;        // weight row within the tile
     const int sub = row >> 7, rr = row & 127;
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           for (int i = 0; i < WPT; ++i) {
             const int chunk = part * WPT + i;
             *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) =
-                dequant_word(cw[i], cs[i / PW]);
+                dequant_word(cw[i], cs[i / PW], magic);
           }
           fence_proxy_async_smem();
           __syncwarp();
