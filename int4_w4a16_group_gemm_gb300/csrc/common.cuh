@@ -137,19 +137,51 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------- numbers
-// `v`, returned through a warp shuffle so that the compiler cannot fold it
-// into an instruction immediate. The nibble unpack computes
-// (word & mask) | 0x4B000000: with both constants as immediates that takes
-// two logic instructions, with the pattern in a register one three-input
-// logic instruction, and the logic pipe is the unpack's bottleneck. All 32
+// `v`, returned through a warp shuffle so that the compiler can neither
+// fold it into an instruction immediate nor re-create it with a move before
+// every use (both cost instructions on the unpack's critical pipes). All 32
 // lanes of the warp must call it together.
 __device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
   return __shfl_sync(0xFFFFFFFFu, v, 0);
 }
+__device__ __forceinline__ float opaque_f32(float v) { return __shfl_sync(0xFFFFFFFFu, v, 0); }
 
-// Exponent pattern of 2^23: OR-ing an integer m < 2^23 into it gives the
-// fp32 number 2^23 + m.
-constexpr uint32_t kMagic2p23 = 0x4B000000u;
+// Nibble unpack to fp32 without integer->float conversions. A packed word
+// holds nibbles n0..n7 (nibble j in bits 4j..4j+3). For c in 0..3 the
+// nibbles c and c+4 are moved into the two fp16 halves of one register:
+//   h = (src & mask_c) | 0x64006400,  src = word (c < 2) or word >> 8 (c >= 2),
+//   mask_c = 0x000F000F (c even) or 0x00F000F0 (c odd),
+// so each half is the fp16 number 1024 + n (c even) or 1024 + 16 n (c odd),
+// exact. One mixed-precision add per half, f32(half) + bias with bias =
+// -1032 (c even) or -1152 (c odd), then gives (n - 8) or 16 (n - 8) as an
+// exact fp32 number; the activations of odd classes are pre-multiplied by
+// 1/16 (an exact scaling). The constants live in registers (NibbleConsts):
+// as immediates the compiler would spend extra instructions on them.
+struct NibbleConsts {
+  uint32_t magic;  // 0x64006400: two fp16 1024.0
+  float bias_even, bias_odd;
+};
+__device__ __forceinline__ NibbleConsts make_nibble_consts() {
+  return {opaque_u32(0x64006400u), opaque_f32(-1032.0f), opaque_f32(-1152.0f)};
+}
+// Both nibbles of class c of `word` as exact fp32 values (n - 8) * (c odd ?
+// 16 : 1), in the low and high halves of a packed fp32 pair.
+template <int C>
+__device__ __forceinline__ uint64_t nibble_pair(uint32_t word, uint32_t word_sh8,
+                                                const NibbleConsts &k) {
+  const uint32_t src = C < 2 ? word : word_sh8;
+  const uint32_t h = (src & ((C & 1) ? 0x00F000F0u : 0x000F000Fu)) | k.magic;
+  const float bias = (C & 1) ? k.bias_odd : k.bias_even;
+  uint64_t r;
+  asm("{\n\t.reg .f16 lo, hi;\n\t.reg .f32 a, b;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.f16 a, lo, %2;\n\tadd.rn.f32.f16 b, hi, %2;\n\tmov.b64 %0, {a, b};\n\t}"
+      : "=l"(r)
+      : "r"(h), "f"(bias));
+  return r;
+}
+// Pre-scale factor of the activation matching a class-c nibble.
+__host__ __device__ constexpr float nibble_prescale(int c) { return (c & 1) ? 0.0625f : 1.0f; }
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }

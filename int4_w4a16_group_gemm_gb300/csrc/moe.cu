@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
   }
   __syncthreads();
 
-  const uint32_t magic = opaque_u32(kMagic2p23);
+  const NibbleConsts nk = make_nibble_consts();
   const int k0 = warp * SLICE + lane * EPL;
   const bool active = k0 < K;
   const int kc = active ? k0 : 0;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
                                        : 0.f);
       }
       float part[RC][MT];
-      rows_dot<MT, WPL>(wd, sv, xr, part, magic);
+      rows_dot<MT, WPL>(wd, sv, xr, part, nk);
       float res[MT];
       warp_reduce_8rows<MT>(part, res, lane);
       if ((lane & 3) == 0) {

@@ -8,13 +8,9 @@
 // multiplied with fp32 FMAs; the per-lane partial is scaled by the group
 // scale, and 8 rows at a time are reduced across the warp in a fixed order.
 //
-// Nibble unpacking without integer->float conversion instructions: nibble j
-// of a word sits in bits 4j..4j+3. For the four nibbles of a 16-bit half,
-// (half & (0xF << 4c)) | 0x4B000000 is the fp32 number 2^23 + nibble*16^c
-// (one logic instruction when the pattern comes in as `magic`, see
-// opaque_u32), so subtracting 2^23 + 8*16^c gives (nibble - 8) * 16^c
-// exactly. The matching activation is pre-multiplied by 16^-c (an exact
-// power-of-two scaling), so each FMA adds the exact product (nibble - 8) * x.
+// Nibbles are unpacked with the fp16 magic-number trick and mixed-precision
+// adds (see nibble_pair in common.cuh): each FMA adds the exact product
+// (nibble - 8) * x, with x pre-scaled by 1/16 for the odd nibble classes.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -30,15 +26,6 @@ constexpr int kRowsPerChunk = 8;
 // use 128 registers (8 rows of packed accumulators per token tile plus the
 // lane's activations).
 __host__ __device__ constexpr int stream_max_threads(int, int = 0) { return 512; }
-
-__device__ __forceinline__ float nib_bias(int c) {
-  // 2^23 + 8 * 16^c, exact in fp32 for c = 0..3
-  return c == 0 ? 8388616.0f : c == 1 ? 8388736.0f : c == 2 ? 8390656.0f : 8421376.0f;
-}
-
-__device__ __forceinline__ float nib_prescale(int c) {
-  return c == 0 ? 1.0f : c == 1 ? 0.0625f : c == 2 ? 0.00390625f : 0.000244140625f;
-}
 
 // Packed fp32 pairs: Blackwell's add/fma.f32x2 do two independent fp32
 // operations (each rounded exactly like the scalar one) per instruction.
@@ -84,7 +71,7 @@ __device__ __forceinline__ void load_x_raw(const void *xrow, int k0, uint4 (&raw
 
 // Convert raw activations to the pre-scaled pairs lane_dot consumes: pair
 // 4*i + c of word i holds columns 8i + c and 8i + 4 + c (the two nibbles of
-// class c in the word's low and high half), times 16^-c.
+// class c in the word's low and high half), times nibble_prescale(c).
 template <int EPL, bool BF16>
 __device__ __forceinline__ void convert_x(const uint4 (&raw)[EPL / 4], uint64_t (&xp)[EPL / 2]) {
   float xr[EPL];
@@ -111,7 +98,8 @@ __device__ __forceinline__ void convert_x(const uint4 (&raw)[EPL / 4], uint64_t 
   for (int i = 0; i < EPL / 8; ++i)
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      xp[4 * i + c] = pack_f32x2(xr[8 * i + c] * nib_prescale(c), xr[8 * i + 4 + c] * nib_prescale(c));
+      xp[4 * i + c] = pack_f32x2(xr[8 * i + c] * nibble_prescale(c),
+                                 xr[8 * i + 4 + c] * nibble_prescale(c));
 }
 
 // Load this lane's EPL activations of token row `xrow` (nullptr -> zeros)
@@ -123,50 +111,17 @@ __device__ __forceinline__ void load_x_slice(const void *xrow, int k0, uint64_t 
   convert_x<EPL, BF16>(raw, xp);
 }
 
-// acc[t] = sum over this lane's EPL columns of (nibble - 8) * x[t], for the
-// WPL words in `wd` (word i holds columns 8i .. 8i+7 of the lane's slice).
-// Per nibble pair: two LOP3 build 2^23 + n*16^c, one add.f32x2 removes the
-// bias exactly, one fma.f32x2 accumulates; the low-half and high-half
-// chains are added once at the end.
-template <int MT, int WPL>
-__device__ __forceinline__ void lane_dot(const uint32_t (&wd)[WPL],
-                                         const uint64_t (&xp)[MT][4 * WPL], float (&acc)[MT],
-                                         uint32_t magic) {
-  uint64_t a[MT];
-#pragma unroll
-  for (int t = 0; t < MT; ++t) a[t] = 0ull;  // (+0.0f, +0.0f)
-#pragma unroll
-  for (int i = 0; i < WPL; ++i) {
-    const uint32_t lo = wd[i];
-    const uint32_t hi = wd[i] >> 16;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float nb = -nib_bias(c);
-      const uint64_t q = add_f32x2(
-          pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | magic),
-                     __uint_as_float((hi & (0xFu << (4 * c))) | magic)),
-          pack_f32x2(nb, nb));
-#pragma unroll
-      for (int t = 0; t < MT; ++t) a[t] = fma_f32x2(q, xp[t][4 * i + c], a[t]);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    float l, h;
-    unpack_f32x2(a[t], l, h);
-    acc[t] = l + h;
-  }
-}
-
 // part[r][t] = scale[r] * sum over this lane's columns of (nibble - 8) * x[t]
 // for the 8 rows of a stage, with the rows interleaved: for every word and
 // nibble class the 8 rows' updates are independent, so 8 FMA chains per
-// token are in flight at once.
+// token are in flight at once. Per word and row: one shift, four logic
+// instructions, eight mixed-precision adds and 4 * MT fma.f32x2.
 template <int MT, int WPL>
 __device__ __forceinline__ void rows_dot(const uint32_t (&wd)[kRowsPerChunk][WPL],
                                          const float (&sv)[kRowsPerChunk],
                                          const uint64_t (&xp)[MT][4 * WPL],
-                                         float (&part)[kRowsPerChunk][MT], uint32_t magic) {
+                                         float (&part)[kRowsPerChunk][MT],
+                                         const NibbleConsts &k) {
   uint64_t a[kRowsPerChunk][MT];
 #pragma unroll
   for (int r = 0; r < kRowsPerChunk; ++r)
@@ -175,19 +130,14 @@ __device__ __forceinline__ void rows_dot(const uint32_t (&wd)[kRowsPerChunk][WPL
 #pragma unroll
   for (int i = 0; i < WPL; ++i) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float nb = -nib_bias(c);
-      const uint64_t bias = pack_f32x2(nb, nb);
+    for (int r = 0; r < kRowsPerChunk; ++r) {
+      const uint32_t w = wd[r][i], w8 = w >> 8;
+      const uint64_t q[4] = {nibble_pair<0>(w, w8, k), nibble_pair<1>(w, w8, k),
+                             nibble_pair<2>(w, w8, k), nibble_pair<3>(w, w8, k)};
 #pragma unroll
-      for (int r = 0; r < kRowsPerChunk; ++r) {
-        const uint32_t lo = wd[r][i];
-        const uint64_t q = add_f32x2(
-            pack_f32x2(__uint_as_float((lo & (0xFu << (4 * c))) | magic),
-                       __uint_as_float(((lo >> 16) & (0xFu << (4 * c))) | magic)),
-            bias);
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int t = 0; t < MT; ++t) a[r][t] = fma_f32x2(q, xp[t][4 * i + c], a[r][t]);
-      }
+        for (int t = 0; t < MT; ++t) a[r][t] = fma_f32x2(q[c], xp[t][4 * i + c], a[r][t]);
     }
   }
 #pragma unroll

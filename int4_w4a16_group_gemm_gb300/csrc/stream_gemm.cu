@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const uint32_t magic = opaque_u32(kMagic2p23);
+    const NibbleConsts nk = make_nibble_consts();
     // This lane's columns and its activations (kept in registers).
     const int k0 = warp * SLICE + lane * EPL;
     const bool active = k0 < K;
@@ -205,12 +205,12 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     if constexpr (kDeferReduce) {
       float prev[RC][MT];
       bool ok = nchunks > 0 && fetch(0, wd, sv);
-      if (ok) rows_dot<MT, WPL>(wd, sv, xr, prev, magic);
+      if (ok) rows_dot<MT, WPL>(wd, sv, xr, prev, nk);
       for (int c = 1; ok && c < nchunks; ++c) {
         ok = fetch(c, wd, sv);
         if (!ok) break;
         float part[RC][MT];
-        rows_dot<MT, WPL>(wd, sv, xr, part, magic);
+        rows_dot<MT, WPL>(wd, sv, xr, part, nk);
         store_sums(c - 1, prev);
 #pragma unroll
         for (int r = 0; r < RC; ++r)
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
       for (int c = 0; c < nchunks; ++c) {
         if (!fetch(c, wd, sv)) break;
         float part[RC][MT];
-        rows_dot<MT, WPL>(wd, sv, xr, part, magic);
+        rows_dot<MT, WPL>(wd, sv, xr, part, nk);
         store_sums(c, part);
       }
     }

@@ -174,18 +174,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // 8 packed nibbles (columns 0..7 of the word) * scale -> 8 bf16 in a uint4.
-// (nibble - 8) is formed exactly as an fp32 (magic-number trick, see the
-// streaming kernel), multiplied by the fp32 scale (one rounding, the
-// format's own product), then rounded once more to bf16.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, uint32_t magic) {
-  const uint32_t hi = w >> 16;
+// (nibble - 8) is formed exactly as an fp32 (see nibble_pair), multiplied by
+// the fp32 scale (one rounding, the format's own product), then rounded
+// once more to bf16.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, const NibbleConsts &k) {
+  const uint32_t w8 = w >> 8;
+  const uint64_t p[4] = {nibble_pair<0>(w, w8, k), nibble_pair<1>(w, w8, k),
+                         nibble_pair<2>(w, w8, k), nibble_pair<3>(w, w8, k)};
   float v[8];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const float bias = c == 0 ? 8388616.0f : c == 1 ? 8388736.0f : c == 2 ? 8390656.0f : 8421376.0f;
-    const float sc = c == 0 ? s : c == 1 ? s * 0.0625f : c == 2 ? s * 0.00390625f : s * 0.000244140625f;
-    v[c] = (__uint_as_float((w & (0xFu << (4 * c))) | magic) - bias) * sc;
-    v[4 + c] = (__uint_as_float((hi & (0xFu << (4 * c))) | magic) - bias) * sc;
+    const float sc = s * nibble_prescale(c);  // exact: a power-of-two scaling
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p[c]));
+    v[c] = lo * sc;
+    v[4 + c] = hi * sc;
   }
   uint4 o;
   o.x = pack_bf16x2(v[0], v[1]);
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------- dequant + epilogue
-    const uint32_t magic = opaque_u32(kMagic2p23);
+    const NibbleConsts nk = make_nibble_consts();
     const int dq = threadIdx.x - 64;                  // 0 .. 32 * DQ_WARPS - 1
     const int row = dq / TPR, part = dq % TPR;        // weight row within the tile
     const int sub = row >> 7, rr = row & 127;
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           for (int i = 0; i < WPT; ++i) {
             const int chunk = part * WPT + i;
             *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) =
-                dequant_word(cw[i], cs[i / PW], magic);
+                dequant_word(cw[i], cs[i / PW], nk);
           }
           fence_proxy_async_smem();
           __syncwarp();
