@@ -10,14 +10,17 @@
 //
 // Steps, all on the device and on one stream (the host reads nothing back):
 //  1. sort:     histogram of expert ids -> exclusive scan (offsets) -> stable
-//               scatter of pair indices p = t*topk + slot (perm);
-//  2. gate/up:  per expert, stream its gate and up rows once; every token of
-//               the expert multiplies them; h = silu(g) * u, stored per
-//               sorted position (bf16 in bf16 mode);
-//  3. down:     per expert, stream its down rows once; o[p] = route_w[p] *
+//               scatter of pair indices p = t*topk + slot (perm); the same
+//               kernel lists the work items (expert, tile of up to MT of its
+//               tokens) in expert order;
+//  2. gate/up:  one CTA per (row block, work item): stream the block's gate
+//               and up rows; h = silu(g) * u for the item's tokens, stored
+//               per sorted position (bf16 in bf16 mode);
+//  3. down:     the same over the down rows; o[p] = route_w[p] *
 //               (h @ W_dn^T), stored per pair;
 //  4. combine:  y[t] = o[t*topk + 0] + o[t*topk + 1] + ... (slot order).
-// Each expert's weights are read once per call whatever its token count.
+// The work items of one expert are adjacent in the grid, so an expert's
+// weights come from HBM once and from L2 for its further token tiles.
 #include <algorithm>
 #include <mutex>
 
@@ -31,9 +34,38 @@ namespace {
 constexpr int kMaxExperts = 8192;
 
 // ------------------------------------------------------------------ 1. sort
+// Exclusive prefix sum of `v` over the block's threads (thread order);
+// `scratch` holds 32 ints. Every thread of the block must call it.
+__device__ int block_exclusive_scan(int v, int *scratch, int lane, int warp, int nt) {
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();  // scratch may still be read by a previous call
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < (nt >> 5) ? scratch[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    scratch[lane] = wi - w;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  return scratch[warp] + incl - v;
+}
+
 __global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t *__restrict__ ids, int n,
                                                         int E, int32_t *__restrict__ offsets,
-                                                        int32_t *__restrict__ perm, int *status) {
+                                                        int32_t *__restrict__ perm, int tile,
+                                                        int32_t *__restrict__ items,
+                                                        int32_t *__restrict__ n_items,
+                                                        int *status) {
   __shared__ int cnt[kMaxExperts];
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -47,39 +79,34 @@ __global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t *__restric
       record_status(status, W4A16_ERR_INVALID_ARG);
   }
   __syncthreads();
-  // exclusive scan of cnt[0..E): each thread owns a contiguous chunk
+  // exclusive scans of cnt[0..E) and of the token tiles per expert: each
+  // thread owns a contiguous chunk of experts
   const int per = (E + nt - 1) / nt;
   const int b = min(E, tid * per), f = min(E, b + per);
-  int local = 0;
-  for (int e = b; e < f; ++e) local += cnt[e];
+  int local = 0, local_t = 0;
+  for (int e = b; e < f; ++e) {
+    local += cnt[e];
+    local_t += (cnt[e] + tile - 1) / tile;
+  }
   const int lane = tid & 31, warp = tid >> 5;
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (nt >> 5) ? warp_tot[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-      if (lane >= o) wi += v;
-    }
-    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
-  }
-  __syncthreads();
-  int run = warp_tot[warp] + incl - local;
+  int run = block_exclusive_scan(local, warp_tot, lane, warp, nt);
+  int item = block_exclusive_scan(local_t, warp_tot, lane, warp, nt);
   for (int e = b; e < f; ++e) {
     const int c = cnt[e];
     offsets[e] = run;
     cnt[e] = run;  // becomes the scatter cursor
     run += c;
+    for (int j = 0; j * tile < c; ++j, ++item) {
+      if (items != nullptr) {
+        items[2 * item] = e;
+        items[2 * item + 1] = j;
+      }
+    }
   }
-  if (tid == nt - 1) offsets[E] = run;  // last thread ends at the total
+  if (tid == nt - 1) {  // the last thread ends at the totals
+    offsets[E] = run;
+    if (n_items != nullptr) *n_items = item;
+  }
   __syncthreads();
   // stable scatter by warp 0, 32 pairs at a time in pair order
   if (warp == 0) {
@@ -105,13 +132,15 @@ __global__ void __launch_bounds__(1024) moe_sort_kernel(const int32_t *__restric
 
 // --------------------------------------------------------- 2./3. expert GEMMs
 struct MoeParams {
-  const void *x;        // gate/up: tokens [T][H]; down: h [n][I] (sorted order)
-  const int32_t *perm;  // sorted position -> pair
+  const void *x;          // gate/up: tokens [T][H]; down: h [n][I] (sorted order)
+  const int32_t *perm;    // sorted position -> pair
   const int32_t *offsets;
-  const float *route_w;  // [n]
-  const int32_t *qw;     // expert-major packed weights
+  const int32_t *items;   // work items: (expert, token tile) pairs
+  const int32_t *n_items;
+  const float *route_w;   // [n]
+  const int32_t *qw;      // expert-major packed weights
   const float *sc;
-  void *out;             // gate/up: h [n][I]; down: o [n][H] fp32 (by pair)
+  void *out;              // gate/up: h [n][I]; down: o [n][H] fp32 (by pair)
   int H, I, topk;
   int nstages;
   int sc_bulk;
@@ -120,45 +149,44 @@ struct MoeParams {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// MODE 0: gate/up + SwiGLU (K = H; a stage holds 4 gate rows and the 4
-//         matching up rows, giving 4 columns of h).
-// MODE 1: down + routing weight (K = I; 8 rows of the down projection).
-// A CTA owns expert blockIdx.y and a range of its stages; the expert's
-// tokens are taken in tiles of MT, and every resident stage serves up to
-// kMoeTiles tiles before it is refilled, so an expert's weights stream from
-// HBM once for up to kMoeTiles * MT tokens (more tokens: further passes).
-// Within a pass the structure is the dense streaming kernel's: bulk copies
-// into a ring of stages, 8 rows per stage, and the last warp to finish a
-// stage refills it and reduces the warps' partial sums in a fixed order.
-constexpr int kMoeTiles = 4;
+// Largest number of weight rows a CTA owns (bounds its table of per-warp
+// row sums).
+constexpr int kMoeRowsPerCta = 128;
 
-template <int MT, int WPL, bool BF16, int MODE>
-__global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_kernel(const MoeParams p) {
+// One CTA = one work item (an expert and a tile of up to MT of its tokens;
+// blockIdx.x) x one block of the expert's rows (blockIdx.y). Consecutive
+// CTAs take the tiles of one expert over the same rows, so those rows come
+// from HBM once. The structure is the dense streaming
+// kernel's: consumer warps own K-slices, the last warp streams 8-row stages
+// into a ring with bulk copies and refills a stage as soon as every consumer
+// has loaded its words, the per-warp row sums go to a table that the whole
+// CTA adds in a fixed order at the end.
+// MODE 0: gate/up (K = H). A stage holds 4 gate rows and the 4 matching up
+//         rows; the epilogue writes h = silu(gate) * up.
+// MODE 1: down (K = I), 8 rows per stage; the epilogue writes
+//         o[pair] = route_w[pair] * (h @ W_dn^T).
+template <int MT, int WPL, bool BF16, int MODE, int MAXW, int MINB>
+__global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoeParams p) {
   constexpr int EPL = 8 * WPL;
   constexpr int SLICE = 32 * EPL;
   constexpr int RC = kRowsPerChunk;
   constexpr int RL = MODE == 0 ? 4 : 8;  // logical output rows per stage
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
-  __shared__ int s_issued;
 
-  const int e = blockIdx.y;
-  const int s0 = p.offsets[e];
-  const int ce = p.offsets[e + 1] - s0;
-  if (ce <= 0) return;
+  const int it = blockIdx.x;
+  if (it >= *p.n_items) return;  // the grid is sized for the most items
+  const int e = p.items[2 * it];
+  const int s0 = p.offsets[e] + p.items[2 * it + 1] * MT;
+  const int mt = min(MT, p.offsets[e + 1] - s0);
 
   const int K = MODE == 0 ? p.H : p.I;
   const int L = MODE == 0 ? p.I : p.H;  // logical rows of the expert
-  const int nlc = (L + RL - 1) / RL;
-  const int c_begin = static_cast<int>((static_cast<long long>(nlc) * blockIdx.x) / gridDim.x);
-  const int c_end = static_cast<int>((static_cast<long long>(nlc) * (blockIdx.x + 1)) / gridDim.x);
-  const int nchunks = c_end - c_begin;
-  if (nchunks <= 0) return;
-  const int ntiles = (ce + MT - 1) / MT;
-  const int npass = (ntiles + kMoeTiles - 1) / kMoeTiles;
-  const int total = nchunks * npass;  // stages over all passes
+  const int l_begin = static_cast<int>((static_cast<long long>(L) * blockIdx.y) / gridDim.y);
+  const int l_end = static_cast<int>((static_cast<long long>(L) * (blockIdx.y + 1)) / gridDim.y);
+  const int nchunks = (l_end - l_begin + RL - 1) / RL;
 
-  const int nw = blockDim.x >> 5;
+  const int nw = (blockDim.x >> 5) - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = K >> 5;
   const uint32_t qrow = static_cast<uint32_t>(K) >> 1;
@@ -170,27 +198,29 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
   const uint8_t *qbase = reinterpret_cast<const uint8_t *>(p.qw) + e * erows * qrow;
   const uint8_t *sbase = reinterpret_cast<const uint8_t *>(p.sc) + e * erows * srow;
 
+  // shared memory: NS stages | full[NS] | empty[NS] | red[nchunks*RC][MT][nw]
   uint8_t *stages = smem;
-  float *red = reinterpret_cast<float *>(smem + NS * stage_bytes);
-  int *count = reinterpret_cast<int *>(red + 2 * NS * kMoeTiles * nw * RC * MT);
-  uint64_t *full = reinterpret_cast<uint64_t *>(count + ((2 * NS + 1) & ~1));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
+  uint64_t *empty = full + NS;
+  float *red = reinterpret_cast<float *>(empty + NS);
 
-  // global row of stage row r for logical chunk starting at l0 (-1: none)
-  auto stage_row = [&](int l0, int r) -> int {
+  // expert row held by stage row r of chunk c (-1: past the block)
+  auto stage_row = [&](int c, int r) -> int {
+    const int l0 = l_begin + c * RL;
     if (MODE == 0) {
       const int j = l0 + (r & 3);
-      if (j >= p.I) return -1;
+      if (j >= l_end) return -1;
       return r < 4 ? j : p.I + j;
     } else {
       const int n = l0 + r;
-      return n < p.H ? n : -1;
+      return n < l_end ? n : -1;
     }
   };
 
-  auto issue = [&](int gc) {  // gc: stage index over all passes
-    const int slot = gc % NS;
-    const int l0 = (c_begin + gc % nchunks) * RL;
-    const int rows = min(RL, L - l0);
+  auto issue = [&](int c) {
+    const int slot = c % NS;
+    const int l0 = l_begin + c * RL;
+    const int rows = min(RL, l_end - l0);
     uint8_t *dst = stages + slot * stage_bytes;
     const int parts = MODE == 0 ? 2 : 1;
     const uint32_t bq = rows * qrow, bs = p.sc_bulk ? rows * srow : 0u;
@@ -202,160 +232,121 @@ __global__ void __launch_bounds__(stream_max_threads(MT, WPL), 1) moe_stream_ker
     }
   };
 
-  if (threadIdx.x == 0) {
+  const int first = min(NS, nchunks);
+  if (threadIdx.x == nw * 32) {
     s_abort = 0;
-    for (int i = 0; i < 2 * NS; ++i) count[i] = 0;
-    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nw);
+    }
     fence_mbar_init();
-    const int first = min(NS, total);
-    for (int gc = 0; gc < first; ++gc) issue(gc);
-    s_issued = first;
+    for (int c = 0; c < first; ++c) issue(c);
   }
   __syncthreads();
 
-  const NibbleConsts nk = make_nibble_consts();
-  const int k0 = warp * SLICE + lane * EPL;
-  const bool active = k0 < K;
-  const int kc = active ? k0 : 0;
-  const int g = kc >> 5;
-
-  uint64_t xr[MT][EPL / 2];
-  auto load_tile = [&](int tile) {
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = first, released = 0;
+      for (int c = 0; c + NS < nchunks; ++c) {
+        if (!mbar_wait_or_abort(&empty[c % NS], static_cast<uint32_t>(c / NS) & 1u, &s_abort)) {
+          if (atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
+          break;
+        }
+        released = c + 1;
+        issue(c + NS);
+        ++issued;
+      }
+      if (static_cast<volatile int &>(s_abort) != 0)
+        for (int d = released; d < issued; ++d)
+          mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const NibbleConsts nk = make_nibble_consts();
+    const int k0 = warp * SLICE + lane * EPL;
+    const bool active = k0 < K;
+    const int kc = active ? k0 : 0;
+    const int g = kc >> 5;
+    uint64_t xr[MT][EPL / 2];
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-      const int q = tile * MT + t;
       const void *row = nullptr;
-      if (active && q < ce) {
-        const int s = s0 + q;
-        if (MODE == 0) {
-          const int tok = p.perm[s] / p.topk;
-          row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
-                                                 static_cast<size_t>(tok) * p.H)
-                     : static_cast<const void *>(static_cast<const float *>(p.x) +
-                                                 static_cast<size_t>(tok) * p.H);
-        } else {
-          row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) +
-                                                 static_cast<size_t>(s) * p.I)
-                     : static_cast<const void *>(static_cast<const float *>(p.x) +
-                                                 static_cast<size_t>(s) * p.I);
-        }
+      if (active && t < mt) {
+        const int s = s0 + t;
+        const size_t xrow = MODE == 0 ? static_cast<size_t>(p.perm[s] / p.topk) * p.H
+                                      : static_cast<size_t>(s) * p.I;
+        row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) + xrow)
+                   : static_cast<const void *>(static_cast<const float *>(p.x) + xrow);
       }
       load_x_slice<EPL, BF16>(row, k0, xr[t]);
     }
-  };
-
-  for (int gc = 0; gc < total; ++gc) {
-    const int pass = gc / nchunks;
-    const int c = gc % nchunks;
-    const int t_begin = pass * kMoeTiles;
-    const int nt = min(kMoeTiles, ntiles - t_begin);
-    if (nt == 1 && c == 0) load_tile(t_begin);  // single tile: x stays in registers
-    const int slot = gc % NS;
-    const int half = (gc / NS) & 1;
-    const int l0 = (c_begin + c) * RL;
-    int ok = 1;
-    if (lane == 0) {
-      ok = (s_abort == 0) && mbar_wait(&full[slot], static_cast<uint32_t>(gc / NS) & 1u);
-      if (!ok && s_abort == 0) {
-        record_status(p.status, W4A16_ERR_TIMEOUT);
-        s_abort = 1;
-      }
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) break;
-    const uint8_t *st = stages + slot * stage_bytes;
-    const uint8_t *wbase = st + (kc >> 1);
-    float *redc = red + (static_cast<size_t>(half * NS + slot) * kMoeTiles) * nw * RC * MT;
-#pragma unroll 1
-    for (int j = 0; j < nt; ++j) {
-      if (nt > 1) load_tile(t_begin + j);
-      // the stage's words and scales, read per tile so that nothing but the
-      // activations stays live across tiles
-      uint32_t wd[RC][WPL];
+    for (int c = 0; c < nchunks; ++c) {
+      const int slot = c % NS;
       float sv[RC];
+      if (!p.sc_bulk) {
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          const int grow = stage_row(c, r);
+          sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
+                                    static_cast<size_t>(grow) * G + g)
+                            : 0.f;
+        }
+      }
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait_or_abort(&full[slot], static_cast<uint32_t>(c / NS) & 1u, &s_abort);
+        if (!ok && atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      const uint8_t *st = stages + slot * stage_bytes;
+      const uint8_t *wbase = st + (kc >> 1);
+      uint32_t wd[RC][WPL];
 #pragma unroll
       for (int r = 0; r < RC; ++r) {
         load_words<WPL>(wbase + r * qrow, wd[r]);
-        const int grow = stage_row(l0, r);
-        sv[r] = p.sc_bulk ? reinterpret_cast<const float *>(st + qstage + r * srow)[g]
-                          : (grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
-                                               static_cast<size_t>(grow) * G + g)
-                                       : 0.f);
+        if (p.sc_bulk) sv[r] = reinterpret_cast<const float *>(st + qstage + r * srow)[g];
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
       float part[RC][MT];
       rows_dot<MT, WPL>(wd, sv, xr, part, nk);
       float res[MT];
       warp_reduce_8rows<MT>(part, res, lane);
       if ((lane & 3) == 0) {
-        const int row = (lane >> 2) & 7;
+        const int row = c * RC + ((lane >> 2) & 7);
 #pragma unroll
-        for (int t = 0; t < MT; ++t) redc[((j * nw + warp) * RC + row) * MT + t] = res[t];
-      }
-    }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&count[half * NS + slot], 1) == nw - 1;
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (!last) continue;
-    // every warp has finished reading this stage: refill it first
-    if (lane == 0) {
-      __threadfence_block();
-      count[half * NS + slot] = 0;
-      if (gc + NS < total && s_abort == 0) {
-        issue(gc + NS);
-        atomicAdd(&s_issued, 1);
-      }
-    }
-    __syncwarp();
-    // fixed-order sum over the warps: lane (row r, part q) adds warps
-    // q, q+4, ... in order, then the four parts pairwise
-    const int r = lane >> 2, q = lane & 3;
-    for (int j = 0; j < nt; ++j) {
-      const int tile = t_begin + j;
-      float v[MT];
-#pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        float a = 0.f;
-        for (int w = q; w < nw; w += 4) a += redc[((j * nw + w) * RC + r) * MT + t];
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
-        v[t] = a;
-      }
-      if (MODE == 0) {
-        // lanes of rows 0-3 hold the gate sums, rows 4-7 the up sums
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const float up = __shfl_down_sync(0xFFFFFFFFu, v[t], 16);
-          const int tq = tile * MT + t;
-          if (q == 0 && r < 4 && l0 + r < p.I && tq < ce) {
-            const float h = silu_f(v[t]) * up;
-            const size_t idx = static_cast<size_t>(s0 + tq) * p.I + l0 + r;
-            if (BF16)
-              static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
-            else
-              static_cast<float *>(p.out)[idx] = h;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const int tq = tile * MT + t;
-          if (q == 0 && l0 + r < p.H && tq < ce) {
-            const int pair = p.perm[s0 + tq];
-            static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l0 + r] =
-                p.route_w[pair] * v[t];
-          }
-        }
+        for (int t = 0; t < MT; ++t) red[(row * MT + t) * nw + warp] = res[t];
       }
     }
   }
+
+  // ------------------------------------------------------------ epilogue
   __syncthreads();
-  if (threadIdx.x == 0 && s_abort != 0) {
-    for (int d = max(0, s_issued - NS); d < s_issued; ++d)
-      mbar_wait(&full[d % NS], static_cast<uint32_t>(d / NS) & 1u);
+  if (static_cast<volatile int &>(s_abort) != 0) return;
+  auto rowsum = [&](int prow, int t) {
+    const float *v = red + static_cast<size_t>(prow * MT + t) * nw;
+    float a = 0.f;
+    for (int w = 0; w < nw; ++w) a += v[w];
+    return a;
+  };
+  const int nl = l_end - l_begin;
+  for (int i = threadIdx.x; i < nl * MT; i += blockDim.x) {
+    const int l = i / MT, t = i - l * MT;
+    if (t >= mt) continue;
+    if (MODE == 0) {
+      const int prow = (l / 4) * RC + (l & 3);
+      const float h = silu_f(rowsum(prow, t)) * rowsum(prow + 4, t);
+      const size_t idx = static_cast<size_t>(s0 + t) * p.I + l_begin + l;
+      if (BF16)
+        static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(h);
+      else
+        static_cast<float *>(p.out)[idx] = h;
+    } else {
+      const int pair = p.perm[s0 + t];
+      static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l_begin + l] =
+          p.route_w[pair] * rowsum(l, t);
+    }
   }
 }
 
@@ -387,40 +378,54 @@ __global__ void moe_combine_kernel(const float *__restrict__ o, const int32_t *_
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t off_offsets, off_perm, off_h, off_o, total;
+  size_t off_offsets, off_perm, off_items, off_nitems, off_h, off_o, total;
 };
+
+// Token tile of the expert kernels (the same for both, since the work items
+// are listed once): 3 tokens with two packed words per lane while both K
+// fit 15 consumer warps, else 1 token with four words per lane.
+constexpr int kMoeKMultiToken = 15 * 512;
+int moe_tile(int H, int I) { return (H <= kMoeKMultiToken && I <= kMoeKMultiToken) ? 3 : 1; }
+
+int moe_max_items(int n, int E, int tile) { return (n + tile - 1) / tile + std::min(n, E); }
 
 WsLayout ws_layout(int T, int topk, int E, int H, int I) {
   const size_t n = static_cast<size_t>(T) * topk;
+  const int tile = moe_tile(H, I);
   WsLayout w{};
   w.off_offsets = 0;
   w.off_perm = align256(sizeof(int32_t) * (E + 1));
-  w.off_h = w.off_perm + align256(sizeof(int32_t) * std::max<size_t>(n, 1));
+  w.off_items = w.off_perm + align256(sizeof(int32_t) * std::max<size_t>(n, 1));
+  w.off_nitems = w.off_items +
+                 align256(sizeof(int32_t) * 2 * std::max(1, moe_max_items(static_cast<int>(n), E, tile)));
+  w.off_h = w.off_nitems + align256(sizeof(int32_t));
   w.off_o = w.off_h + align256(sizeof(float) * n * I);
   w.total = w.off_o + align256(sizeof(float) * n * H);
   return w;
 }
 
-template <int MT, int WPL, bool BF16, int MODE>
-cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
-                               cudaStream_t stream) {
+template <int MT, int WPL, bool BF16, int MODE, int MAXW, int MINB>
+cudaError_t launch_expert_kernel(MoeParams p, int K, int L, int max_items, const DeviceInfo &di,
+                                 cudaStream_t stream) {
   constexpr int SLICE = 32 * 8 * WPL;
   const int nw = (K + SLICE - 1) / SLICE;
-  const int threads = nw * 32;
+  if (nw + 1 > MAXW) return cudaErrorInvalidConfiguration;
+  const int threads = (nw + 1) * 32;
+  const int RL = MODE == 0 ? 4 : 8;
+  // row blocks of at most kMoeRowsPerCta weight rows
+  const int gx = std::max(1, (L * (kRowsPerChunk / RL) + kMoeRowsPerCta - 1) / kMoeRowsPerCta);
+  const int lrows = (L + gx - 1) / gx;
+  const int chunks = (lrows + RL - 1) / RL;
   const size_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
+  const size_t table = static_cast<size_t>(chunks) * kRowsPerChunk * MT * nw * sizeof(float);
   const size_t budget = static_cast<size_t>(di.smem_optin) - 1024;
-  auto bytes_for = [&](int ns) {
-    return static_cast<size_t>(ns) * stage +
-           2ull * ns * kMoeTiles * nw * kRowsPerChunk * MT * sizeof(float) +
-           (2 * ns + 2) * sizeof(int) + ns * sizeof(uint64_t) + 64;
-  };
-  // three stages keep two CTAs per SM resident for the widest experts
-  int ns = 3;
+  auto bytes_for = [&](int ns) { return ns * stage + 2ull * ns * sizeof(uint64_t) + table; };
+  int ns = std::min(3, chunks);
   while (ns > 1 && bytes_for(ns) > budget) --ns;
   if (bytes_for(ns) > budget) return cudaErrorInvalidConfiguration;
   p.nstages = ns;
   const size_t smem = bytes_for(ns);
-  auto kern = moe_stream_kernel<MT, WPL, BF16, MODE>;
+  auto kern = moe_expert_kernel<MT, WPL, BF16, MODE, MAXW, MINB>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -428,25 +433,21 @@ cudaError_t launch_expert_pass(MoeParams p, int K, int E, const DeviceInfo &di,
                                     static_cast<int>(budget));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  // split every expert into several CTAs so the active experts spread
-  // evenly over the SMs (empty experts exit at once)
-  const int per_expert = 8;
-  dim3 grid(per_expert, E);
-  kern<<<grid, threads, smem, stream>>>(p);
+  kern<<<dim3(max_items, gx), threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_expert(MoeParams p, bool bf16, int K, int E, const DeviceInfo &di,
+cudaError_t launch_expert(MoeParams p, bool bf16, int tile, int max_items, const DeviceInfo &di,
                           cudaStream_t stream) {
+  const int K = MODE == 0 ? p.H : p.I;
+  const int L = MODE == 0 ? p.I : p.H;
   p.sc_bulk = (K % 128 == 0) ? 1 : 0;
-  // token tiles of 3 (bf16) or 2 (fp32, whose wider activation registers
-  // would not fit 3) with two packed words per lane up to K = 8192
-  if (K <= max_k_stream(3))
-    return bf16 ? launch_expert_pass<3, 2, true, MODE>(p, K, E, di, stream)
-                : launch_expert_pass<2, 2, false, MODE>(p, K, E, di, stream);
-  return bf16 ? launch_expert_pass<1, 4, true, MODE>(p, K, E, di, stream)
-              : launch_expert_pass<1, 4, false, MODE>(p, K, E, di, stream);
+  if (tile == 3)
+    return bf16 ? launch_expert_kernel<3, 2, true, MODE, 16, 1>(p, K, L, max_items, di, stream)
+                : launch_expert_kernel<3, 2, false, MODE, 16, 1>(p, K, L, max_items, di, stream);
+  return bf16 ? launch_expert_kernel<1, 4, true, MODE, 17, 1>(p, K, L, max_items, di, stream)
+              : launch_expert_kernel<1, 4, false, MODE, 17, 1>(p, K, L, max_items, di, stream);
 }
 
 }  // namespace
@@ -454,7 +455,8 @@ cudaError_t launch_expert(MoeParams p, bool bf16, int K, int E, const DeviceInfo
 cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *offsets,
                             int32_t *perm, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
-  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n_pairs, E, offsets, perm, di.status);
+  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n_pairs, E, offsets, perm, 1, nullptr, nullptr,
+                                          di.status);
   return cudaGetLastError();
 }
 
@@ -471,16 +473,24 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.off_offsets);
   int32_t *perm = reinterpret_cast<int32_t *>(ws + L.off_perm);
+  int32_t *items = reinterpret_cast<int32_t *>(ws + L.off_items);
+  int32_t *n_items = reinterpret_cast<int32_t *>(ws + L.off_nitems);
   void *h = ws + L.off_h;
   float *o = reinterpret_cast<float *>(ws + L.off_o);
   const int n = T * topk;
+  const int tile = moe_tile(H, I);
+  const int max_items = moe_max_items(n, E, tile);
 
-  cudaError_t err = launch_moe_sort(ids, n, E, offsets, perm, stream);
+  moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n, E, offsets, perm, tile, items, n_items,
+                                          di.status);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   MoeParams p{};
   p.perm = perm;
   p.offsets = offsets;
+  p.items = items;
+  p.n_items = n_items;
   p.route_w = route_w;
   p.H = H;
   p.I = I;
@@ -491,14 +501,14 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
   p.qw = qw_gu;
   p.sc = sc_gu;
   p.out = h;
-  err = launch_expert<0>(p, x_bf16, H, E, di, stream);
+  err = launch_expert<0>(p, x_bf16, tile, max_items, di, stream);
   if (err != cudaSuccess) return err;
 
   p.x = h;
   p.qw = qw_dn;
   p.sc = sc_dn;
   p.out = o;
-  err = launch_expert<1>(p, x_bf16, I, E, di, stream);
+  err = launch_expert<1>(p, x_bf16, tile, max_items, di, stream);
   if (err != cudaSuccess) return err;
 
   const long long work = static_cast<long long>(T) * (H / 4);

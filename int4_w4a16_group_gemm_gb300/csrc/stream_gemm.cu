@@ -263,12 +263,11 @@ cudaError_t launch_tiles(const StreamParams &base, int tiles, int N, int K, int 
   const size_t stage = kRowsPerChunk * (K / 2 + (SCB ? K / 8 : 0));
   static const int env_ns = env_int("W4A16_STREAM_NS");
   static const int env_ctas = env_int("W4A16_STREAM_CTAS");
-  // One row block per SM (more when a block would exceed kMaxRowsPerCta
-  // rows). With MINB == 2 the CTA is sized (registers and shared memory) so
-  // that a CTA of the next call on the stream fits beside it: under
-  // programmatic launch that CTA starts its weight stream while this one
-  // computes.
-  const int ctas_per_sm = env_ctas > 0 ? std::min(env_ctas, 4) : 1;
+  // MINB row blocks per SM (more when a block would exceed kMaxRowsPerCta
+  // rows). The unpack is bound by instruction issue: two CTAs of 14
+  // consumer warps keep all four schedulers of an SM equally busy, which
+  // beats one CTA with the next call's CTA resident beside it.
+  const int ctas_per_sm = env_ctas > 0 ? std::min(env_ctas, 4) : MINB;
   int gx = std::min((N + kRowsPerChunk - 1) / kRowsPerChunk, nsm * ctas_per_sm);
   gx = std::max({1, gx, (N + kMaxRowsPerCta - 1) / kMaxRowsPerCta});
   const int rows_per_cta = (N + gx - 1) / gx;
@@ -367,9 +366,8 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
   const int tiles = (M + mt - 1) / mt;
   const int nsm = di.num_sms, opt = di.smem_optin;
   // One token: lanes own two packed words per row (16 columns) up to
-  // K = 7680, four beyond. Up to K = 7168 the CTA (14 consumer warps and the
-  // producer, at most 64 registers a thread) leaves room for a CTA of the
-  // next call.
+  // K = 7680, four beyond. Up to K = 7168 two CTAs (14 consumer warps and
+  // the producer each, at most 64 registers a thread) share an SM.
   if (mt == 1 && K <= 7168)
     return x_bf16 ? launch_tiles_sc<1, 2, true, 15, 2>(p, tiles, N, K, nsm, opt, overlap, stream)
                   : launch_tiles_sc<1, 2, false, 15, 2>(p, tiles, N, K, nsm, opt, overlap, stream);
