@@ -23,6 +23,7 @@
 // weights come from HBM once and from L2 for its further token tiles.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "stream_core.cuh"
@@ -263,62 +264,73 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // The tile's token count selects the code path, so a tile of one or two
+    // tokens does not pay for three.
     const NibbleConsts nk = make_nibble_consts();
     const int k0 = warp * SLICE + lane * EPL;
     const bool active = k0 < K;
     const int kc = active ? k0 : 0;
     const int g = kc >> 5;
-    uint64_t xr[MT][EPL / 2];
+    auto consume = [&](auto tokens) {
+      constexpr int TM = decltype(tokens)::value;
+      uint64_t xr[TM][EPL / 2];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      const void *row = nullptr;
-      if (active && t < mt) {
-        const int s = s0 + t;
-        const size_t xrow = MODE == 0 ? static_cast<size_t>(p.perm[s] / p.topk) * p.H
-                                      : static_cast<size_t>(s) * p.I;
-        row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) + xrow)
-                   : static_cast<const void *>(static_cast<const float *>(p.x) + xrow);
+      for (int t = 0; t < TM; ++t) {
+        const void *row = nullptr;
+        if (active && t < mt) {
+          const int s = s0 + t;
+          const size_t xrow = MODE == 0 ? static_cast<size_t>(p.perm[s] / p.topk) * p.H
+                                        : static_cast<size_t>(s) * p.I;
+          row = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) + xrow)
+                     : static_cast<const void *>(static_cast<const float *>(p.x) + xrow);
+        }
+        load_x_slice<EPL, BF16>(row, k0, xr[t]);
       }
-      load_x_slice<EPL, BF16>(row, k0, xr[t]);
-    }
-    for (int c = 0; c < nchunks; ++c) {
-      const int slot = c % NS;
-      float sv[RC];
-      if (!p.sc_bulk) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int slot = c % NS;
+        float sv[RC];
+        if (!p.sc_bulk) {
+#pragma unroll
+          for (int r = 0; r < RC; ++r) {
+            const int grow = stage_row(c, r);
+            sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
+                                      static_cast<size_t>(grow) * G + g)
+                              : 0.f;
+          }
+        }
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait_or_abort(&full[slot], static_cast<uint32_t>(c / NS) & 1u, &s_abort);
+          if (!ok && atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+        const uint8_t *st = stages + slot * stage_bytes;
+        const uint8_t *wbase = st + (kc >> 1);
+        uint32_t wd[RC][WPL];
 #pragma unroll
         for (int r = 0; r < RC; ++r) {
-          const int grow = stage_row(c, r);
-          sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
-                                    static_cast<size_t>(grow) * G + g)
-                            : 0.f;
+          load_words<WPL>(wbase + r * qrow, wd[r]);
+          if (p.sc_bulk) sv[r] = reinterpret_cast<const float *>(st + qstage + r * srow)[g];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        float part[RC][TM];
+        rows_dot<TM, WPL>(wd, sv, xr, part, nk);
+        float res[TM];
+        warp_reduce_8rows<TM>(part, res, lane);
+        if ((lane & 3) == 0) {
+          const int row = c * RC + ((lane >> 2) & 7);
+#pragma unroll
+          for (int t = 0; t < TM; ++t) red[(row * MT + t) * nw + warp] = res[t];
         }
       }
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait_or_abort(&full[slot], static_cast<uint32_t>(c / NS) & 1u, &s_abort);
-        if (!ok && atomicExch(&s_abort, 1) == 0) record_status(p.status, W4A16_ERR_TIMEOUT);
-      }
-      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-      const uint8_t *st = stages + slot * stage_bytes;
-      const uint8_t *wbase = st + (kc >> 1);
-      uint32_t wd[RC][WPL];
-#pragma unroll
-      for (int r = 0; r < RC; ++r) {
-        load_words<WPL>(wbase + r * qrow, wd[r]);
-        if (p.sc_bulk) sv[r] = reinterpret_cast<const float *>(st + qstage + r * srow)[g];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-      float part[RC][MT];
-      rows_dot<MT, WPL>(wd, sv, xr, part, nk);
-      float res[MT];
-      warp_reduce_8rows<MT>(part, res, lane);
-      if ((lane & 3) == 0) {
-        const int row = c * RC + ((lane >> 2) & 7);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) red[(row * MT + t) * nw + warp] = res[t];
-      }
-    }
+    };
+    if (MT >= 3 && mt >= 3)
+      consume(std::integral_constant<int, (MT >= 3 ? 3 : 1)>{});
+    else if (MT >= 2 && mt == 2)
+      consume(std::integral_constant<int, (MT >= 2 ? 2 : 1)>{});
+    else
+      consume(std::integral_constant<int, 1>{});
   }
 
   // ------------------------------------------------------------ epilogue
