@@ -532,7 +532,8 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = pk["source"]
-    roof["traffic"] = profiled_traffic(f"config{args.config}")
+    roof["traffic"] = profiled_traffic(
+        f"config{args.config}" + (f"_{args.dtype}" if args.config == 2 else ""))
 
     if rank != 0:
         return 0
