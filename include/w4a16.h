@@ -95,8 +95,8 @@ enum {
    * just before it is still running; it reads x and writes y only after
    * that kernel has completed. The caller guarantees that the kernel
    * launched just before does not write qw or sc (true when weights are
-   * prepared earlier, as in a decode loop). Used by the streaming kernel;
-   * ignored by the tensor-core kernel. */
+   * prepared earlier, as in a decode loop). Both kernels honour it: the
+   * tensor-core kernel dequantises its first stages of weights early. */
   W4A16_FLAG_OVERLAP = 1u
 };
 

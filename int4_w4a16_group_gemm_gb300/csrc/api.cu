@@ -115,7 +115,8 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
   const bool bf16 = xdt == W4A16_ACT_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc)
-    return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y, s));
+    return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y,
+                                    (flags & W4A16_FLAG_OVERLAP) != 0, s));
   return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N,
                                       (flags & W4A16_FLAG_OVERLAP) != 0, s));
 }

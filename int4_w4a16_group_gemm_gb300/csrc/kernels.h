@@ -42,9 +42,10 @@ int stream_tile(int M, int K);
 int stream_gemm_passes(int M, int K);
 
 // ------------------------------------------------------------ tensor-core kernel
-// Same contract for bf16 activations on tcgen05 tensor cores.
+// Same contract for bf16 activations on tcgen05 tensor cores, including
+// `overlap`.
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M,
-                           int N, int K, float *y, cudaStream_t stream);
+                           int N, int K, float *y, bool overlap, cudaStream_t stream);
 bool tc_gemm_supported(int M, int N, int K);
 
 // ------------------------------------------------------------ quantiser

@@ -274,6 +274,11 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic launch: let the next kernel on the stream start launching
+  // now. Only the weights (never written by the previous kernel, by the
+  // overlap contract) are read before griddep_wait; x and y after it. Both
+  // calls are no-ops for a kernel launched without the attribute.
+  griddep_launch_dependents();
 
   auto fail = [&]() {
     record_status(p.status, W4A16_ERR_TIMEOUT);
@@ -283,6 +288,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
+      griddep_wait();
       int it = 0;
       for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag); tile += tile_step) {
         const int m0 = (tile % p.tiles_m) * BM;
@@ -420,6 +426,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         }
       }
       if (!ok) break;
+      griddep_wait();  // before the first write of y
       // -------- epilogue: accumulator esub, TMEM lanes q*32 .. q*32+31
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full, static_cast<uint32_t>(tcount) & 1u))) {
         fail();
@@ -462,6 +469,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
   }
   __syncthreads();
   if (SPLIT) {
+    griddep_wait();  // every thread writes y below
     // every CTA of the cluster has parked its partial tile
     cluster_sync_all();
     const int n0 = (tile_first / p.tiles_m) * ROWS;
@@ -527,7 +535,7 @@ namespace {
 
 template <int BM, int SUBS, bool SPLIT>
 cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, int ks,
-                      cudaStream_t stream) {
+                      bool overlap, cudaStream_t stream) {
   using Cfg = TcCfg<BM, SUBS>;
   auto kern = tc_gemm_kernel<BM, SUBS, SPLIT>;
   static std::once_flag attr_once;
@@ -541,13 +549,15 @@ cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, in
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = SPLIT ? ks : 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmap, p);
 }
 
@@ -559,7 +569,7 @@ int env_int(const char *name) {
 }  // namespace
 
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
-                           int K, float *y, cudaStream_t stream) {
+                           int K, float *y, bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
@@ -594,9 +604,10 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
     const int kmax = env_ks > 0 ? std::min(env_ks, 8) : 4;
     const int nk = (K + TC_BK - 1) / TC_BK;
     const int ks = std::max(1, std::min(std::min(kmax, nk), di.num_sms / std::max(1, p.num_tiles)));
-    return launch_tc<64, 1, true>(tmap, p, p.num_tiles, ks, stream);
+    return launch_tc<64, 1, true>(tmap, p, p.num_tiles, ks, overlap, stream);
   }
-  return launch_tc<256, 2, false>(tmap, p, std::min(p.num_tiles, di.num_sms), 1, stream);
+  return launch_tc<256, 2, false>(tmap, p, std::min(p.num_tiles, di.num_sms), 1, overlap,
+                                   stream);
 }
 
 }  // namespace w4a16

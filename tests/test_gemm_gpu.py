@@ -237,3 +237,57 @@ def test_cuda_core_path_rejects_k_beyond_its_limit(w4):
     with pytest.raises(w4.W4A16Error) as ei:
         w4.w4a16_gemm(x, qw, sc)
     assert ei.value.code == w4.W4A16_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M", [64, 300])
+def test_tensor_core_overlap_chain(w4, M):
+    """The tensor-core kernel under W4A16_FLAG_OVERLAP (split-K at M = 64,
+    persistent tiles at M = 300): a chain of bf16 GEMMs, each consuming the
+    previous output, into NaN-poisoned buffers gives the same bits as the
+    plain chain; the first link is checked against the oracle."""
+    K = 2048
+    x = synth.activations(14, M, K)
+    ws = [synth.weights(14, K, K, sub=i) for i in range(3)]
+    dev = [w4.w4a16_quantize(torch.from_numpy(w).cuda()) for w in ws]
+
+    def chain(overlap):
+        ins = [torch.full((M, K), float("nan"), device="cuda", dtype=torch.bfloat16) for _ in dev]
+        outs = [torch.full((M, K), float("nan"), device="cuda") for _ in dev]
+        torch.cuda.synchronize()
+        ins[0].copy_(torch.from_numpy(x).to(torch.bfloat16))
+        for i, (qw, sc) in enumerate(dev):
+            w4.w4a16_gemm(ins[i], qw, sc, y=outs[i], algo="tc", overlap=overlap)
+            if i + 1 < len(dev):
+                ins[i + 1].copy_(outs[i].to(torch.bfloat16))
+        torch.cuda.synchronize()
+        return outs
+
+    plain = chain(False)
+    over = chain(True)
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    for a, b in zip(plain, over):
+        assert torch.isfinite(a).all()
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    xo = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    q0, c0 = oracle.quantize_w4a16(ws[0])
+    ref, bound = oracle.gemm_ref(xo, q0, c0)
+    assert np.all(np.abs(plain[0].cpu().numpy().astype(np.float64) - ref) <= TOL["bf16"] * bound)
+
+
+@pytest.mark.parametrize("M", [64, 300])
+def test_tensor_core_overlap_back_to_back_same_output(w4, M):
+    """Back-to-back overlapped tensor-core calls writing the same y (a
+    write-after-write chain with no other kernel between them) leave the
+    last call's result."""
+    N, K = 4096, 2048
+    x = torch.from_numpy(synth.activations(15, M, K)).to(torch.bfloat16).cuda()
+    qa, sa = w4.w4a16_quantize(torch.from_numpy(synth.weights(15, N, K, sub=0)).cuda())
+    qb, sb = w4.w4a16_quantize(torch.from_numpy(synth.weights(15, N, K, sub=1)).cuda())
+    ref_b = w4.w4a16_gemm(x, qb, sb, algo="tc")
+    y = torch.empty((M, N), device="cuda")
+    for _ in range(5):
+        w4.w4a16_gemm(x, qa, sa, y=y, algo="tc", overlap=True)
+        w4.w4a16_gemm(x, qb, sb, y=y, algo="tc", overlap=True)
+    torch.cuda.synchronize()
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    assert torch.equal(y.view(torch.int32), ref_b.view(torch.int32))
