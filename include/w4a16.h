@@ -68,7 +68,10 @@ typedef enum {
 typedef enum {
   W4A16_ALGO_AUTO = 0,   /* pick by M and dtype (what w4a16_gemm does) */
   W4A16_ALGO_SIMT = 1,   /* streaming CUDA-core kernel, any M, both dtypes */
-  W4A16_ALGO_TC = 2      /* tcgen05 tensor-core kernel, bf16 activations */
+  W4A16_ALGO_TC = 2      /* tcgen05 tensor-core kernel: bf16 activations, or
+                            fp32 activations with M <= 64 and K <= 16384
+                            (each activation split exactly into three bf16
+                            pieces, group scales applied in fp32) */
 } w4a16_algo;
 
 /*
@@ -80,8 +83,11 @@ typedef enum {
  *   group must be 32; K must be a positive multiple of 32; M, N > 0.
  * fp32 mode keeps every output within 1e-5 * sum_k |x*W_hat| of the exact
  * product; bf16 mode within 4e-3 of it (exact product of the bf16 values).
+ * Kernels: bf16 with M >= 32 runs on the tensor cores; fp32 with
+ * 16 <= M <= 64 on the tensor cores in the fp32-exact split form; the rest
+ * on the streaming CUDA-core kernel.
  * Errors: INVALID_ARG, UNSUPPORTED (group != 32; K > 16384 on the CUDA-core
- * path, i.e. fp32 activations or small M), ALIGNMENT, CUDA.
+ * and fp32 tensor-core paths), ALIGNMENT, CUDA.
  */
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt,
                         const int32_t *qw, const float *sc,
@@ -95,14 +101,15 @@ enum {
    * just before it is still running; it reads x and writes y only after
    * that kernel has completed. The caller guarantees that the kernel
    * launched just before does not write qw or sc (true when weights are
-   * prepared earlier, as in a decode loop). Both kernels honour it: the
-   * tensor-core kernel dequantises its first stages of weights early. */
+   * prepared earlier, as in a decode loop). Every kernel honours it: the
+   * tensor-core kernels dequantise their first stages of weights early. */
   W4A16_FLAG_OVERLAP = 1u
 };
 
 /* w4a16_gemm with an explicit kernel choice and launch flags (0 = none);
- * W4A16_ALGO_TC requires bf16 activations (UNSUPPORTED otherwise). Same
- * arguments and errors as w4a16_gemm, plus INVALID_ARG for unknown flags. */
+ * W4A16_ALGO_TC takes bf16 activations, or fp32 activations with M <= 64
+ * and K <= 16384 (UNSUPPORTED otherwise). Same arguments and errors as
+ * w4a16_gemm, plus INVALID_ARG for unknown flags. */
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt,
                            const int32_t *qw, const float *sc,
                            int M, int N, int K, int group,

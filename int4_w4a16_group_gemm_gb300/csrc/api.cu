@@ -70,35 +70,47 @@ static inline w4a16_status from_cuda(cudaError_t e) {
 
 // M at or above which bf16 activations go to the tensor-core kernel.
 static constexpr int kTcMinM = 32;
+// M range in which fp32 activations go to the fp32-exact tensor-core kernel.
+static constexpr int kTcF32MinM = 16;
+
+enum class GemmKernel { Stream, TensorBf16, TensorF32 };
 
 // Kernel choice shared by the launch path and the launch-count query.
-// Returns OK and sets *use_tc, or the rejection status.
+// Returns OK and sets *kind, or the rejection status.
 static w4a16_status plan_gemm(int M, int N, int K, int group, w4a16_act_dtype xdt,
-                              w4a16_algo algo, bool *use_tc) {
+                              w4a16_algo algo, GemmKernel *kind) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
   if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
   if (algo != W4A16_ALGO_AUTO && algo != W4A16_ALGO_SIMT && algo != W4A16_ALGO_TC)
     return W4A16_ERR_INVALID_ARG;
   if (group != 32) return W4A16_ERR_UNSUPPORTED;
   const bool bf16 = xdt == W4A16_ACT_BF16;
-  *use_tc = false;
+  const bool f32_tc_ok = !bf16 && tc_f32_supported(M, N, K) && K <= max_k_stream(1);
+  *kind = GemmKernel::Stream;
   if (algo == W4A16_ALGO_TC) {
-    if (!bf16 || !tc_gemm_supported(M, N, K)) return W4A16_ERR_UNSUPPORTED;
-    *use_tc = true;
+    if (bf16 && tc_gemm_supported(M, N, K))
+      *kind = GemmKernel::TensorBf16;
+    else if (f32_tc_ok)
+      *kind = GemmKernel::TensorF32;
+    else
+      return W4A16_ERR_UNSUPPORTED;
   } else if (algo == W4A16_ALGO_AUTO) {
-    *use_tc = bf16 && M >= kTcMinM && tc_gemm_supported(M, N, K);
+    if (bf16 && M >= kTcMinM && tc_gemm_supported(M, N, K))
+      *kind = GemmKernel::TensorBf16;
+    else if (f32_tc_ok && M >= kTcF32MinM)
+      *kind = GemmKernel::TensorF32;
   }
-  if (!*use_tc && K > max_k_stream(1)) return W4A16_ERR_UNSUPPORTED;
+  if (*kind == GemmKernel::Stream && K > max_k_stream(1)) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
 }
 
 extern "C" {
 
 int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt, w4a16_algo algo) {
-  bool use_tc = false;
-  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &use_tc);
+  GemmKernel kind;
+  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &kind);
   if (st != W4A16_OK) return -static_cast<int>(st);
-  return use_tc ? 1 : stream_gemm_passes(M, K);
+  return kind == GemmKernel::Stream ? stream_gemm_passes(M, K) : 1;
 }
 
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw,
@@ -106,19 +118,22 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
                            w4a16_algo algo, unsigned int flags, w4a16_stream_t stream) {
   if (!x || !qw || !sc || !y) return W4A16_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned int>(W4A16_FLAG_OVERLAP)) return W4A16_ERR_INVALID_ARG;
-  bool use_tc = false;
-  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &use_tc);
+  GemmKernel kind;
+  const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &kind);
   if (st != W4A16_OK) return st;
   if (!aligned16(x) || !aligned16(qw) || !aligned16(sc) || !aligned16(y))
     return W4A16_ERR_ALIGNMENT;
   if (!device_ready()) return W4A16_ERR_CUDA;
   const bool bf16 = xdt == W4A16_ACT_BF16;
+  const bool overlap = (flags & W4A16_FLAG_OVERLAP) != 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (use_tc)
-    return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y,
-                                    (flags & W4A16_FLAG_OVERLAP) != 0, s));
-  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N,
-                                      (flags & W4A16_FLAG_OVERLAP) != 0, s));
+  if (kind == GemmKernel::TensorBf16)
+    return from_cuda(
+        launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y, overlap, s));
+  if (kind == GemmKernel::TensorF32)
+    return from_cuda(
+        launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, y, overlap, s));
+  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N, overlap, s));
 }
 
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *qw, const float *sc,

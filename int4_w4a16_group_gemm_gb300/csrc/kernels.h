@@ -47,6 +47,12 @@ int stream_gemm_passes(int M, int K);
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M,
                            int N, int K, float *y, bool overlap, cudaStream_t stream);
 bool tc_gemm_supported(int M, int N, int K);
+// fp32 activations on the tensor cores, exact to fp32 accumulation: each
+// activation is split into three bf16 pieces and the group scales are
+// applied in fp32 outside the MMA (M <= 64).
+cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, int M, int N,
+                          int K, float *y, bool overlap, cudaStream_t stream);
+bool tc_f32_supported(int M, int N, int K);
 
 // ------------------------------------------------------------ quantiser
 cudaError_t launch_quantize(const float *w, int N, int K, int32_t *qw, float *sc,

@@ -157,13 +157,37 @@ def test_tensor_core_path(w4, M, N, K):
     run_case(w4, M, N, K, "bf16", seed=M + N + K, algo="tc")
 
 
-def test_tensor_core_path_rejects_fp32(w4):
-    x = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+def test_tensor_core_path_rejects_fp32_beyond_64_tokens(w4):
+    x = torch.zeros((65, 64), dtype=torch.float32, device="cuda")
     qw = torch.zeros((8, 8), dtype=torch.int32, device="cuda")
     sc = torch.zeros((8, 2), dtype=torch.float32, device="cuda")
     with pytest.raises(w4.W4A16Error) as ei:
         w4.w4a16_gemm(x, qw, sc, algo="tc")
     assert ei.value.code == w4.W4A16_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M,N,K,outlier", [
+    (64, 4096, 7168, 0.01), (64, 7168, 2048, 0.01), (33, 300, 160, 0.0), (17, 1000, 4128, 0.0),
+    (64, 13, 96, 0.0), (1, 256, 64, 0.0), (5, 129, 2080, 0.0), (64, 128, 32, 0.0),
+    (40, 520, 16384, 0.01),
+])
+def test_fp32_tensor_core_path(w4, M, N, K, outlier):
+    """The fp32-exact tensor-core kernel (activations split into three bf16
+    pieces, group scales applied in fp32) against the fp32 tolerance 1e-5 of
+    sum|x * W_hat|: tree-verify shapes with outliers, ragged N and K (a
+    single group, a last stage holding one group), M = 1 and the largest K."""
+    _, ratio = run_case(w4, M, N, K, "f32", seed=M * 7 + N + K, outlier=outlier, algo="tc")
+    assert ratio < 0.1  # far inside the bound, as fp32 accumulation should be
+
+
+def test_fp32_tensor_core_deterministic_and_auto_choice(w4):
+    M, N, K = 64, 700, 3072
+    x = torch.from_numpy(synth.activations(16, M, K)).cuda()
+    qw, sc = w4.w4a16_quantize(torch.from_numpy(synth.weights(16, N, K)).cuda())
+    a = w4.w4a16_gemm(x, qw, sc, algo="tc")
+    b = w4.w4a16_gemm(x, qw, sc)  # M = 64 fp32: the automatic choice is the same kernel
+    assert w4.w4a16_gemm_launches(M, N, K, "f32", "auto") == 1
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
 def test_tensor_core_deterministic(w4):
