@@ -83,8 +83,8 @@ typedef enum {
  *   group must be 32; K must be a positive multiple of 32; M, N > 0.
  * fp32 mode keeps every output within 1e-5 * sum_k |x*W_hat| of the exact
  * product; bf16 mode within 4e-3 of it (exact product of the bf16 values).
- * Kernels: bf16 with M >= 32 runs on the tensor cores; fp32 with
- * 16 <= M <= 64 on the tensor cores in the fp32-exact split form; the rest
+ * Kernels: bf16 with M >= 4 runs on the tensor cores; fp32 with
+ * 12 <= M <= 64 on the tensor cores in the fp32-exact split form; the rest
  * on the streaming CUDA-core kernel.
  * Errors: INVALID_ARG, UNSUPPORTED (group != 32; K > 16384 on the CUDA-core
  * and fp32 tensor-core paths), ALIGNMENT, CUDA.

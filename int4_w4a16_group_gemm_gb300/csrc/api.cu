@@ -68,10 +68,12 @@ static inline w4a16_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
-// M at or above which bf16 activations go to the tensor-core kernel.
-static constexpr int kTcMinM = 32;
-// M range in which fp32 activations go to the fp32-exact tensor-core kernel.
-static constexpr int kTcF32MinM = 16;
+// M at or above which bf16 activations go to the tensor-core kernel, and
+// from which (up to 64) fp32 activations go to the fp32-exact tensor-core
+// kernel: the crossovers against the streaming kernel measured on the
+// decode-sized weight (N = 4096, K = 7168).
+static constexpr int kTcMinM = 4;
+static constexpr int kTcF32MinM = 12;
 
 enum class GemmKernel { Stream, TensorBf16, TensorF32 };
 
