@@ -11,7 +11,7 @@
 //   * (nib - 8) is a small integer, exact in bf16.
 // The products (nib - 8) * x_i are exact, the tensor cores add them in fp32
 // into TMEM, one 32-column group at a time (three MMAs per 16 columns, one
-// per activation piece), and readback warps multiply each group's sum by
+// per activation piece) into a ring of four accumulators, and readback warps multiply each group's sum by
 // its fp32 scale and accumulate in registers. The scale never passes through
 // bf16, so the result carries only fp32 summation error. The summation depth
 // per output is the 32 columns of a group inside the tensor core, the
@@ -23,7 +23,10 @@
 // kernel reuses. Stage = 64 columns (two groups):
 //   A   16 KB  (nib - 8) in bf16, canonical K-major 128-byte swizzle
 //   B   3 x 8 KB  the activation pieces, same layout
-//   X   16 KB  the fp32 activation tile, loaded by TMA (no swizzle)
+// in a ring of 3 MMA stages, and the fp32 activation tiles (16 KB, loaded
+// by TMA without swizzle) in a separate ring of 4 that the dequantisers
+// release as soon as they have split a tile, so activation loads run ahead
+// of the MMAs.
 // Within every 8-column word the K order of A and B is (0,4,1,5,2,6,3,7):
 // the bf16 magic-number unpack yields nibbles c and c+4 together, and a
 // contraction is unchanged by one permutation of K applied to both operands.
@@ -64,11 +67,13 @@ constexpr int FX_THREADS = 64 + 32 * (FX_DQ_WARPS + FX_RB_WARPS);
 constexpr int FX_A_BYTES = FX_ROWS * FX_BK * 2;  // 16 KB
 constexpr int FX_B_BYTES = FX_BM * FX_BK * 2;    // 8 KB per piece
 constexpr int FX_X_BYTES = FX_BM * FX_BK * 4;    // 16 KB
-constexpr int FX_STAGE = FX_A_BYTES + 3 * FX_B_BYTES + FX_X_BYTES;
-constexpr int FX_NS = 3;
+constexpr int FX_STAGE = FX_A_BYTES + 3 * FX_B_BYTES;  // one MMA stage
+constexpr int FX_NS = 3;            // MMA stages
+constexpr int FX_NSX = 4;           // fp32 activation tiles in flight
 constexpr int FX_PD = 2;            // stages of packed weights prefetched per thread
-constexpr int FX_TMEM_COLS = 128;   // two 64-column group accumulators
-constexpr int FX_SMEM = FX_NS * FX_STAGE + 1024 + 256;
+constexpr int FX_ACC = 4;           // group accumulators in TMEM (64 columns each)
+constexpr int FX_TMEM_COLS = FX_ACC * 64;
+constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + 1024 + 256;
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
 // N = 64, M = 128.
 constexpr uint32_t FX_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -132,12 +137,14 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * SB);  // A and B written
-  uint64_t *xfull = full + NS;                                     // fp32 tile landed
-  uint64_t *empty = xfull + NS;                                    // MMAs of the stage done
-  uint64_t *acc_full = empty + NS;                                 // [2] group sum ready
-  uint64_t *acc_empty = acc_full + 2;                              // [2] group sum read
-  uint64_t *drain = acc_empty + 2;
+  uint8_t *xring = smem + NS * SB;                                 // fp32 activation tiles
+  uint64_t *full = reinterpret_cast<uint64_t *>(xring + FX_NSX * FX_X_BYTES);  // A, B written
+  uint64_t *xfull = full + NS;                                     // [FX_NSX] tile landed
+  uint64_t *xempty = xfull + FX_NSX;                               // [FX_NSX] tile split
+  uint64_t *empty = xempty + FX_NSX;                               // MMAs of the stage done
+  uint64_t *acc_full = empty + NS;                                 // [FX_ACC] group sum ready
+  uint64_t *acc_empty = acc_full + FX_ACC;                         // [FX_ACC] group sum read
+  uint64_t *drain = acc_empty + FX_ACC;
   uint64_t *recv_bar = drain + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -159,10 +166,13 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], FX_DQ_WARPS);
-      mbar_init(&xfull[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int x = 0; x < FX_NSX; ++x) {
+      mbar_init(&xfull[x], 1);
+      mbar_init(&xempty[x], FX_DQ_WARPS);
+    }
+    for (int b = 0; b < FX_ACC; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], FX_RB_WARPS);
     }
@@ -197,18 +207,17 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     if (lane == 0) {
       griddep_wait();
       for (int kb = kb0, it = 0; kb < kb1 && !aborted(abort_flag); ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
-        mbar_arrive_expect_tx(&xfull[s], FX_X_BYTES);
-        tma_load_2d(smem + s * SB + FX_A_BYTES + 3 * FX_B_BYTES, &tmap_x, kb * FX_BK, 0,
-                    &xfull[s]);
+        const int x = it % FX_NSX;
+        const uint32_t ph = static_cast<uint32_t>(it / FX_NSX) & 1u;
+        if (!mbar_wait(&xempty[x], ph ^ 1u)) { fail(); break; }
+        mbar_arrive_expect_tx(&xfull[x], FX_X_BYTES);
+        tma_load_2d(xring + x * FX_X_BYTES, &tmap_x, kb * FX_BK, 0, &xfull[x]);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      int g = 0;  // group counter: buffer g & 1, use g >> 1
+      int g = 0;  // group counter: buffer g % FX_ACC, use g / FX_ACC
       bool issued_any = false;
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
         const int s = it % NS;
@@ -220,8 +229,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         const int groups = min(2, (K >> 5) - 2 * kb);  // the last stage may hold one group
         bool ok = true;
         for (int h = 0; h < groups; ++h, ++g) {
-          const int buf = g & 1;
-          if (!mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u) ||
+          const int buf = g % FX_ACC;
+          if (!mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(g / FX_ACC) & 1u) ^ 1u) ||
               aborted(abort_flag)) {
             fail();
             ok = false;
@@ -283,6 +292,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         if (kb >= kb1) break;
         const int s = it % NS;
         const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+        const int xs = it % FX_NSX;
+        const uint32_t xph = static_cast<uint32_t>(it / FX_NSX) & 1u;
         ++it;
         uint32_t cw[4];
 #pragma unroll
@@ -291,14 +302,14 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         // the slot is free, then the activation tile has landed
         int got = 1;
         if (lane == 0)
-          got = mbar_wait(&empty[s], ph ^ 1u) && mbar_wait(&xfull[s], ph) && !aborted(abort_flag);
+          got = mbar_wait(&empty[s], ph ^ 1u) && mbar_wait(&xfull[xs], xph) && !aborted(abort_flag);
         if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { fail(); ok = false; break; }
         uint8_t *st = smem + s * SB;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4 *>(st + sw128_offset(arow, apart * 4 + i)) =
               dequant_word_int(cw[i], magic, bias);
-        const float *xt = reinterpret_cast<const float *>(st + FX_A_BYTES + 3 * FX_B_BYTES);
+        const float *xt = reinterpret_cast<const float *>(xring + xs * FX_X_BYTES);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int chunk = bpair * 2 + j;
@@ -314,7 +325,10 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (lane == 0) {
+          mbar_arrive(&full[s]);
+          mbar_arrive(&xempty[xs]);  // this warp has split its part of the tile
+        }
       }
     }
   } else {
@@ -333,8 +347,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     for (int gk = g_begin, g = 0; gk < g_end; ++gk, ++g) {
       const float s = s_next;
       s_next = (nvalid && gk + 1 < g_end) ? __ldg(srow + gk + 1) : 0.f;
-      const int buf = g & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], static_cast<uint32_t>(g >> 1) & 1u))) {
+      const int buf = g % FX_ACC;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], static_cast<uint32_t>(g / FX_ACC) & 1u))) {
         fail();
         ok = false;
         break;
@@ -354,12 +368,13 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     }
     if (ok) {
       // partial tile to shared memory (the pipeline stages are idle once
-      // every group has been read), row-major with the 16-byte chunks of a
-      // row rotated by the row index
+      // every group has been read), row-major with the elements of row r
+      // rotated by r (column m at (m + r) mod 64): conflict-free for 32
+      // consecutive rows at one column
       float *red = reinterpret_cast<float *>(smem);
 #pragma unroll
       for (int m = 0; m < FX_BM; ++m)
-        red[r * FX_BM + ((((m >> 2) ^ r) & (FX_BM / 4 - 1)) << 2) + (m & 3)] = acc[m];
+        red[r * FX_BM + ((m + r) & (FX_BM - 1))] = acc[m];
       fence_proxy_async_smem();  // the bulk copies read `red`
     }
   }
@@ -388,7 +403,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         const int i = e % my_rows, m = e / my_rows;
         const int nl = lo + i;
         if (n0 + nl >= p.N || m >= p.M) continue;
-        const int col = ((((m >> 2) ^ nl) & (FX_BM / 4 - 1)) << 2) + (m & 3);
+        const int col = (m + nl) & (FX_BM - 1);
         float v = recv[i * FX_BM + col];
         for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * FX_BM + col];
         p.y[static_cast<size_t>(m) * p.N + n0 + nl] = v;

@@ -347,9 +347,10 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         const int nl = esub * 128 + q * 32 + lane;  // row within the tile
         const int ne = n0 + nl;
         const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + esub * BM;
-        // split: partial tile to shared memory, row-major with the 16-byte
-        // chunks of each row rotated by the row index (the lanes of a warp,
-        // 32 consecutive rows, then hit different banks); the stages are idle
+        // split: partial tile to shared memory, row-major with the elements
+        // of each row rotated by the row index (column m of row r at
+        // (m + r) mod BM), so that the 32 lanes of a warp, 32 consecutive
+        // rows at one column, hit 32 different banks; the stages are idle
         float *red = reinterpret_cast<float *>(smem);
 #pragma unroll 1
         for (int cc = 0; cc < BM / 32; ++cc) {
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int m = cc * 32 + j;
-              red[nl * BM + ((((m >> 2) ^ nl) & (BM / 4 - 1)) << 2) + (m & 3)] = __uint_as_float(r[j]);
+              red[nl * BM + ((m + nl) & (BM - 1))] = __uint_as_float(r[j]);
             }
           } else {
             const int mb = m0 + cc * 32;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         const int i = e % my_rows, m = e / my_rows;  // consecutive threads: consecutive rows
         const int nl = lo + i;
         if (n0 + nl >= p.N || m0 + m >= p.M) continue;
-        const int col = ((((m >> 2) ^ nl) & (BM / 4 - 1)) << 2) + (m & 3);
+        const int col = (m + nl) & (BM - 1);
         float v = recv[i * BM + col];
         for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * BM + col];
         p.y[static_cast<size_t>(m0 + m) * p.N + n0 + nl] = v;
