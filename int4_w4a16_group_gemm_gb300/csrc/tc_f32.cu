@@ -23,10 +23,10 @@
 // kernel reuses. Stage = 64 columns (two groups):
 //   A   16 KB  (nib - 8) in bf16, canonical K-major 128-byte swizzle
 //   B   3 x 8 KB  the activation pieces, same layout
-// in a ring of 3 MMA stages, and the fp32 activation tiles (16 KB, loaded
-// by TMA without swizzle) in a separate ring of 4 that the dequantisers
-// release as soon as they have split a tile, so activation loads run ahead
-// of the MMAs.
+// in a ring of 4 MMA stages, and the fp32 activation tiles (16 KB, loaded
+// by TMA as two 128-byte-swizzled halves) in a separate ring of 3 that the
+// dequantisers release as soon as they have split a tile, so activation
+// loads run ahead of the MMAs.
 // Within every 8-column word the K order of A and B is (0,4,1,5,2,6,3,7):
 // the bf16 magic-number unpack yields nibbles c and c+4 together, and a
 // contraction is unchanged by one permutation of K applied to both operands.
@@ -68,8 +68,8 @@ constexpr int FX_A_BYTES = FX_ROWS * FX_BK * 2;  // 16 KB
 constexpr int FX_B_BYTES = FX_BM * FX_BK * 2;    // 8 KB per piece
 constexpr int FX_X_BYTES = FX_BM * FX_BK * 4;    // 16 KB
 constexpr int FX_STAGE = FX_A_BYTES + 3 * FX_B_BYTES;  // one MMA stage
-constexpr int FX_NS = 3;            // MMA stages
-constexpr int FX_NSX = 4;           // fp32 activation tiles in flight
+constexpr int FX_NS = 4;            // MMA stages
+constexpr int FX_NSX = 3;           // fp32 activation tiles in flight
 constexpr int FX_PD = 2;            // stages of packed weights prefetched per thread
 constexpr int FX_ACC = 4;           // group accumulators in TMEM (64 columns each)
 constexpr int FX_TMEM_COLS = FX_ACC * 64;
@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         const uint32_t ph = static_cast<uint32_t>(it / FX_NSX) & 1u;
         if (!mbar_wait(&xempty[x], ph ^ 1u)) { fail(); break; }
         mbar_arrive_expect_tx(&xfull[x], FX_X_BYTES);
+        // two 32-column boxes (128-byte rows, 128-byte swizzle)
         tma_load_2d(xring + x * FX_X_BYTES, &tmap_x, kb * FX_BK, 0, &xfull[x]);
+        tma_load_2d(xring + x * FX_X_BYTES + FX_X_BYTES / 2, &tmap_x, kb * FX_BK + 32, 0,
+                    &xfull[x]);
       }
     }
   } else if (warp == 1) {
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     const int n = n0 + arow;
     const bool nvalid = n < p.N;
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.qw) + static_cast<size_t>(n) * Kw;
-    const int bm = dq >> 2, bpair = dq & 3;           // B: token, pair of 16-byte chunks
+    const int bm = dq & 63, bpair = dq >> 6;          // B: token, pair of 16-byte chunks
     // register ring of PD prefetched stages of 4 packed words; a word past
     // K or past N holds nibbles 8 (value 0)
     uint32_t ra[PD][4];
@@ -309,12 +312,16 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4 *>(st + sw128_offset(arow, apart * 4 + i)) =
               dequant_word_int(cw[i], magic, bias);
-        const float *xt = reinterpret_cast<const float *>(xring + xs * FX_X_BYTES);
+        // the fp32 tile: two [64 tokens][32 columns] halves, 16-byte pieces
+        // of each 128-byte row swizzled by the row index
+        const uint8_t *xt = xring + xs * FX_X_BYTES;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int chunk = bpair * 2 + j;
-          const float4 lo = *reinterpret_cast<const float4 *>(xt + bm * FX_BK + chunk * 8);
-          const float4 hi = *reinterpret_cast<const float4 *>(xt + bm * FX_BK + chunk * 8 + 4);
+          const uint8_t *xrow = xt + (chunk >> 2) * (FX_X_BYTES / 2) + bm * 128;
+          const int p0 = (chunk & 3) * 2;  // first 16-byte piece of the chunk
+          const float4 lo = *reinterpret_cast<const float4 *>(xrow + ((p0 ^ (bm & 7)) << 4));
+          const float4 hi = *reinterpret_cast<const float4 *>(xrow + (((p0 + 1) ^ (bm & 7)) << 4));
           const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
           uint4 o1, o2, o3;
           split_chunk(v, o1, o2, o3);
@@ -440,10 +447,10 @@ cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, in
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 4};
-  const cuuint32_t box[2] = {FX_BK, FX_BM};
+  const cuuint32_t box[2] = {FX_BK / 2, FX_BM};  // 128-byte rows
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   FxParams p{};
