@@ -10,10 +10,11 @@
 //     three 8-bit pieces);
 //   * (nib - 8) is a small integer, exact in bf16.
 // The products (nib - 8) * x_i are exact, the tensor cores add them in fp32
-// into TMEM, one 32-column group at a time (three MMAs per 16 columns, one
-// per activation piece) into a ring of four accumulators, and readback warps multiply each group's sum by
-// its fp32 scale and accumulate in registers. The scale never passes through
-// bf16, so the result carries only fp32 summation error. The summation depth
+// into TMEM, one 32-column group at a time (one MMA per 16 columns with the
+// three pieces side by side as N = 192) into a ring of two accumulators,
+// readback warps add the three pieces' sums in fp32, multiply each group's
+// sum by its fp32 scale and accumulate in registers. The scale never passes
+// through bf16, so the result carries only fp32 summation error. The depth
 // per output is the 32 columns of a group inside the tensor core, the
 // CTA's groups (an fp32 FMA chain, at most 128 for K <= 16384), then the
 // split-K partials of the cluster in rank order.
@@ -71,13 +72,14 @@ constexpr int FX_STAGE = FX_A_BYTES + 3 * FX_B_BYTES;  // one MMA stage
 constexpr int FX_NS = 4;            // MMA stages
 constexpr int FX_NSX = 3;           // fp32 activation tiles in flight
 constexpr int FX_PD = 2;            // stages of packed weights prefetched per thread
-constexpr int FX_ACC = 4;           // group accumulators in TMEM (64 columns each)
-constexpr int FX_TMEM_COLS = FX_ACC * 64;
+constexpr int FX_NB = 3 * FX_BM;    // MMA N: the three activation pieces side by side
+constexpr int FX_ACC = 2;           // group accumulators in TMEM (FX_NB columns each)
+constexpr int FX_TMEM_COLS = 512;   // FX_ACC * FX_NB rounded up to a power of two
 constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + 1024 + 256;
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
-// N = 64, M = 128.
+// N = 192 (the three 64-row piece tiles are one K-major B tile), M = 128.
 constexpr uint32_t FX_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
-                              (static_cast<uint32_t>(FX_BM >> 3) << 17) |
+                              (static_cast<uint32_t>(FX_NB >> 3) << 17) |
                               (static_cast<uint32_t>(FX_ROWS >> 4) << 24);
 
 struct FxParams {
@@ -240,13 +242,11 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
             break;
           }
           tc_fence_after();
+          // one MMA per 16 columns covers the three pieces: A is read once
 #pragma unroll
-          for (int piece = 0; piece < 3; ++piece)
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              tc_mma(tmem + buf * FX_BM, sw128_desc(a0 + (2 * h + k) * 32),
-                     sw128_desc(b0 + piece * FX_B_BYTES + (2 * h + k) * 32), FX_IDESC,
-                     (piece > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 2; ++k)
+            tc_mma(tmem + buf * FX_NB, sw128_desc(a0 + (2 * h + k) * 32),
+                   sw128_desc(b0 + (2 * h + k) * 32), FX_IDESC, k > 0 ? 1u : 0u);
           tc_commit(&acc_full[buf]);
           issued_any = true;
         }
@@ -361,13 +361,22 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * FX_BM;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * FX_NB;
+      // the group sum is the three pieces' sums added in fp32
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t d[32];
-        tmem_ld_32cols(taddr + half * 32, d);
+      for (int part = 0; part < FX_BM / 16; ++part) {
+        uint32_t d[16];
+        float t[16];
+        tmem_ld_16cols(taddr + part * 16, d);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[half * 32 + j] = fmaf(s, __uint_as_float(d[j]), acc[half * 32 + j]);
+        for (int j = 0; j < 16; ++j) t[j] = __uint_as_float(d[j]);
+        tmem_ld_16cols(taddr + FX_BM + part * 16, d);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t[j] += __uint_as_float(d[j]);
+        tmem_ld_16cols(taddr + 2 * FX_BM + part * 16, d);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          acc[part * 16 + j] = fmaf(s, t[j] + __uint_as_float(d[j]), acc[part * 16 + j]);
       }
       tc_fence_before();
       __syncwarp();
