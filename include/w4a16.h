@@ -7,11 +7,13 @@
  * and section "Input Knowledge Required": symmetric per-group INT4 weights,
  * 8 nibbles packed per int32 along the input dimension (K), stored value
  * nibble = q + 8 (so the weight is nibble - 8), one fp32 scale per group of
- * 32 consecutive input columns. Within a word, input column k sits in bits
- * 4*(k mod 8) .. 4*(k mod 8)+3 (low nibble first).
- *   qw[N][K/8]  int32   row n = output feature, K-contiguous
- *   sc[N][K/32] float   scale of (row n, group k/32)
- *   W_hat[n][k] = (nibble(n,k) - 8) * sc[n][k/32]
+ * `group` consecutive input columns: 32 is the size the pages fix; 64 and
+ * 128 (the other common W4A16 group sizes) are taken too. Within a word,
+ * input column k sits in bits 4*(k mod 8) .. 4*(k mod 8)+3 (low nibble
+ * first).
+ *   qw[N][K/8]      int32   row n = output feature, K-contiguous
+ *   sc[N][K/group]  float   scale of (row n, group k/group)
+ *   W_hat[n][k] = (nibble(n,k) - 8) * sc[n][k/group]
  *
  * Operation. "The Silence of Success: A Single Line That Speaks Volumes",
  * section "What the Edit Actually Built": activations (fp32; a bf16 mode is
@@ -51,9 +53,11 @@ typedef struct CUstream_st *w4a16_stream_t;
 
 typedef enum {
   W4A16_OK = 0,
-  W4A16_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, K % 32 != 0,
-                                bad enum, workspace too small, id out of range */
-  W4A16_ERR_UNSUPPORTED = 2, /* group != 32, or a size beyond a kernel limit */
+  W4A16_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, K not a
+                                multiple of the group, bad enum, workspace
+                                too small, id out of range */
+  W4A16_ERR_UNSUPPORTED = 2, /* group not 32, 64 or 128, or a size beyond a
+                                kernel limit */
   W4A16_ERR_ALIGNMENT = 3,   /* a pointer not 16-byte aligned */
   W4A16_ERR_CUDA = 4,        /* a CUDA runtime or launch error */
   W4A16_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out */
@@ -78,15 +82,15 @@ typedef enum {
  * w4a16_gemm - y = x * W_hat^T.
  *   x   [M][K]   fp32 or bf16 (xdt), device, 16-byte aligned
  *   qw  [N][K/8] int32 packed nibbles, device, 16-byte aligned
- *   sc  [N][K/32] fp32 scales, device, 16-byte aligned
+ *   sc  [N][K/group] fp32 scales, device, 16-byte aligned
  *   y   [M][N]   fp32 output, device, 16-byte aligned (overwritten)
- *   group must be 32; K must be a positive multiple of 32; M, N > 0.
+ *   group is 32, 64 or 128; K a positive multiple of group; M, N > 0.
  * fp32 mode keeps every output within 1e-5 * sum_k |x*W_hat| of the exact
  * product; bf16 mode within 4e-3 of it (exact product of the bf16 values).
  * Kernels: bf16 with M >= 4 runs on the tensor cores; fp32 with
  * 12 <= M <= 64 on the tensor cores in the fp32-exact split form; the rest
  * on the streaming CUDA-core kernel.
- * Errors: INVALID_ARG, UNSUPPORTED (group != 32; K > 16384 on the CUDA-core
+ * Errors: INVALID_ARG, UNSUPPORTED (group not 32/64/128; K > 16384 on the CUDA-core
  * and fp32 tensor-core paths), ALIGNMENT, CUDA.
  */
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt,
@@ -129,8 +133,10 @@ int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt,
  * device:  s = max|w| / 7 (fp32 division), q = clamp(round-half-even(w / s),
  * -8, 7) (q = 0 when s = 0), nibble = q + 8, packed low nibble first.
  *   w  [N][K]    fp32 input (finite values), device
- *   qw [N][K/8]  int32 output, device;  sc [N][K/32] fp32 output, device
- * Errors: INVALID_ARG, UNSUPPORTED (group != 32), ALIGNMENT (qw or w not 16-byte aligned), CUDA.
+ *   qw [N][K/8]  int32 output, device;  sc [N][K/group] fp32 output, device
+ *   group 32, 64 or 128; K a multiple of 32 and of group.
+ * Errors: INVALID_ARG, UNSUPPORTED (group not 32/64/128), ALIGNMENT (qw or
+ * w not 16-byte aligned), CUDA.
  */
 w4a16_status w4a16_quantize(const float *w, int N, int K, int group,
                             int32_t *qw, float *sc, w4a16_stream_t stream);
@@ -166,12 +172,12 @@ size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I);
  * once per call whatever its token count.
  *   x        [T][H] fp32 or bf16 (xdt)
  *   expert_ids [T][topk] int32;  route_w [T][topk] fp32
- *   qw_gu [E][2I][H/8] int32;  sc_gu [E][2I][H/32] fp32
- *   qw_dn [E][H][I/8]  int32;  sc_dn [E][H][I/32]  fp32
+ *   qw_gu [E][2I][H/8] int32;  sc_gu [E][2I][H/group] fp32
+ *   qw_dn [E][H][I/8]  int32;  sc_dn [E][H][I/group]  fp32
  *   workspace: device memory of at least w4a16_moe_workspace_size() bytes,
  *   16-byte aligned, owned by the caller; contents on entry are ignored.
  *   y [T][H] fp32 output (overwritten).
- * group must be 32; H and I multiples of 32, at most 16384.
+ * group is 32, 64 or 128; H and I multiples of group, at most 16384.
  */
 w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt,
                             const int32_t *expert_ids, const float *route_w,

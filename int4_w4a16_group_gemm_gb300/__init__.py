@@ -158,14 +158,14 @@ def w4a16_gemm_raw(x_ptr, xdt, qw_ptr, sc_ptr, M, N, K, group, y_ptr, algo=0, fl
 
 
 def w4a16_quantize(w, group: int = 32, qw=None, sc=None, stream=None):
-    """Quantise fp32 w[N, K] on the device -> (qw int32 [N, K/8], sc fp32 [N, K/32])."""
+    """Quantise fp32 w[N, K] on the device -> (qw int32 [N, K/8], sc fp32 [N, K/group])."""
     import torch
     _need(w, torch.float32, "w")
     N, K = w.shape
     if qw is None:
         qw = torch.empty((N, K // 8), dtype=torch.int32, device=w.device)
     if sc is None:
-        sc = torch.empty((N, K // 32), dtype=torch.float32, device=w.device)
+        sc = torch.empty((N, K // group), dtype=torch.float32, device=w.device)
     code = lib.w4a16_quantize(_ptr(w), N, K, group, _ptr(qw), _ptr(sc), _stream_handle(stream))
     _check("w4a16_quantize", code)
     return qw, sc

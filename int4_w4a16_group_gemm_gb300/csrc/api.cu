@@ -64,6 +64,10 @@ static inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// Group sizes the kernels take: a lane's or a piece's columns (16 or 32)
+// always lie inside one group.
+static inline bool group_supported(int group) { return group == 32 || group == 64 || group == 128; }
+
 static inline w4a16_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
@@ -85,7 +89,8 @@ static w4a16_status plan_gemm(int M, int N, int K, int group, w4a16_act_dtype xd
   if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
   if (algo != W4A16_ALGO_AUTO && algo != W4A16_ALGO_SIMT && algo != W4A16_ALGO_TC)
     return W4A16_ERR_INVALID_ARG;
-  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  if (!group_supported(group)) return W4A16_ERR_UNSUPPORTED;
+  if (K % group != 0) return W4A16_ERR_INVALID_ARG;
   const bool bf16 = xdt == W4A16_ACT_BF16;
   const bool f32_tc_ok = !bf16 && tc_f32_supported(M, N, K) && K <= max_k_stream(1);
   *kind = GemmKernel::Stream;
@@ -131,11 +136,11 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kind == GemmKernel::TensorBf16)
     return from_cuda(
-        launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, y, overlap, s));
+        launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, group, y, overlap, s));
   if (kind == GemmKernel::TensorF32)
     return from_cuda(
-        launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, y, overlap, s));
-  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, y, N, overlap, s));
+        launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, group, y, overlap, s));
+  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, group, y, N, overlap, s));
 }
 
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *qw, const float *sc,
@@ -147,10 +152,12 @@ w4a16_status w4a16_quantize(const float *w, int N, int K, int group, int32_t *qw
                             w4a16_stream_t stream) {
   if (!w || !qw || !sc) return W4A16_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
-  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  if (!group_supported(group)) return W4A16_ERR_UNSUPPORTED;
+  if (K % group != 0) return W4A16_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(qw)) return W4A16_ERR_ALIGNMENT;
   if (!device_ready()) return W4A16_ERR_CUDA;
-  return from_cuda(launch_quantize(w, N, K, qw, sc, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(
+      launch_quantize(w, N, K, group, qw, sc, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_moe_sort(const int32_t *expert_ids, int n_pairs, int E, int32_t *offsets,
@@ -178,7 +185,8 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *e
   if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return W4A16_ERR_INVALID_ARG;
   if (H % 32 != 0 || I % 32 != 0) return W4A16_ERR_INVALID_ARG;
   if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
-  if (group != 32) return W4A16_ERR_UNSUPPORTED;
+  if (!group_supported(group)) return W4A16_ERR_UNSUPPORTED;
+  if (H % group != 0 || I % group != 0) return W4A16_ERR_INVALID_ARG;
   if (E > 8192 || H > max_k_stream(1) || I > max_k_stream(1)) return W4A16_ERR_UNSUPPORTED;
   if (ws_bytes < moe_workspace_bytes(T, topk, E, H, I)) return W4A16_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(qw_gu) || !aligned16(sc_gu) || !aligned16(qw_dn) ||
@@ -186,7 +194,7 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *e
     return W4A16_ERR_ALIGNMENT;
   if (!device_ready()) return W4A16_ERR_CUDA;
   return from_cuda(launch_moe(x, xdt == W4A16_ACT_BF16, expert_ids, route_w, T, topk, qw_gu,
-                              sc_gu, qw_dn, sc_dn, E, H, I, workspace, y,
+                              sc_gu, qw_dn, sc_dn, E, H, I, group, workspace, y,
                               reinterpret_cast<cudaStream_t>(stream)));
 }
 

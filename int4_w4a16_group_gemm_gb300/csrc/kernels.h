@@ -31,8 +31,8 @@ bool take_injected_fault();
 // programmatic stream serialisation: the weight stream may start before the
 // previous kernel on the stream has finished (x and y stay ordered).
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
-                               const float *sc, int M, int N, int K, float *y, int ldy,
-                               bool overlap, cudaStream_t stream);
+                               const float *sc, int M, int N, int K, int group, float *y,
+                               int ldy, bool overlap, cudaStream_t stream);
 // Largest K the streaming kernel accepts for a token tile of `mt` (1, 2, 3).
 int max_k_stream(int mt);
 // Token tile width the streaming kernel uses for M tokens.
@@ -45,17 +45,17 @@ int stream_gemm_passes(int M, int K);
 // Same contract for bf16 activations on tcgen05 tensor cores, including
 // `overlap`.
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M,
-                           int N, int K, float *y, bool overlap, cudaStream_t stream);
+                           int N, int K, int group, float *y, bool overlap, cudaStream_t stream);
 bool tc_gemm_supported(int M, int N, int K);
 // fp32 activations on the tensor cores, exact to fp32 accumulation: each
 // activation is split into three bf16 pieces and the group scales are
 // applied in fp32 outside the MMA (M <= 64).
 cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, int M, int N,
-                          int K, float *y, bool overlap, cudaStream_t stream);
+                          int K, int group, float *y, bool overlap, cudaStream_t stream);
 bool tc_f32_supported(int M, int N, int K);
 
 // ------------------------------------------------------------ quantiser
-cudaError_t launch_quantize(const float *w, int N, int K, int32_t *qw, float *sc,
+cudaError_t launch_quantize(const float *w, int N, int K, int group, int32_t *qw, float *sc,
                             cudaStream_t stream);
 
 // ------------------------------------------------------------ MoE
@@ -65,6 +65,6 @@ size_t moe_workspace_bytes(int T, int topk, int E, int H, int I);
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
                        int T, int topk, const int32_t *qw_gu, const float *sc_gu,
                        const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
-                       void *workspace, float *y, cudaStream_t stream);
+                       int group, void *workspace, float *y, cudaStream_t stream);
 
 }  // namespace w4a16

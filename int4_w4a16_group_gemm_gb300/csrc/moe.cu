@@ -144,6 +144,8 @@ struct MoeParams {
   void *out;              // gate/up: h [n][I]; down: o [n][H] fp32 (by pair)
   int H, I, topk;
   int nstages;
+  int gs;       // log2 of the group size
+  int srow;     // bytes per scale row: (K / group) * 4, K the reduced dimension
   int sc_bulk;
   int *status;
 };
@@ -189,9 +191,8 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 
   const int nw = (blockDim.x >> 5) - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = K >> 5;
   const uint32_t qrow = static_cast<uint32_t>(K) >> 1;
-  const uint32_t srow = static_cast<uint32_t>(K) >> 3;
+  const uint32_t srow = static_cast<uint32_t>(p.srow);
   const uint32_t qstage = RC * qrow;
   const uint32_t stage_bytes = qstage + (p.sc_bulk ? RC * srow : 0u);
   const int NS = p.nstages;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
     const int k0 = warp * SLICE + lane * EPL;
     const bool active = k0 < K;
     const int kc = active ? k0 : 0;
-    const int g = kc >> 5;
+    const int g = kc >> p.gs;
     auto consume = [&](auto tokens) {
       constexpr int TM = decltype(tokens)::value;
       uint64_t xr[TM][EPL / 2];
@@ -293,8 +294,8 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 #pragma unroll
           for (int r = 0; r < RC; ++r) {
             const int grow = stage_row(c, r);
-            sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(sbase) +
-                                      static_cast<size_t>(grow) * G + g)
+            sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(
+                                          sbase + static_cast<size_t>(grow) * srow) + g)
                               : 0.f;
           }
         }
@@ -428,7 +429,7 @@ cudaError_t launch_expert_kernel(MoeParams p, int K, int L, int max_items, const
   const int gx = std::max(1, (L * (kRowsPerChunk / RL) + kMoeRowsPerCta - 1) / kMoeRowsPerCta);
   const int lrows = (L + gx - 1) / gx;
   const int chunks = (lrows + RL - 1) / RL;
-  const size_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? K / 8 : 0));
+  const size_t stage = kRowsPerChunk * (K / 2 + (p.sc_bulk ? (K >> p.gs) * 4 : 0));
   const size_t table = static_cast<size_t>(chunks) * kRowsPerChunk * MT * nw * sizeof(float);
   const size_t budget = static_cast<size_t>(di.smem_optin) - 1024;
   auto bytes_for = [&](int ns) { return ns * stage + 2ull * ns * sizeof(uint64_t) + table; };
@@ -454,7 +455,8 @@ cudaError_t launch_expert(MoeParams p, bool bf16, int tile, int max_items, const
                           cudaStream_t stream) {
   const int K = MODE == 0 ? p.H : p.I;
   const int L = MODE == 0 ? p.I : p.H;
-  p.sc_bulk = (K % 128 == 0) ? 1 : 0;
+  p.srow = (K >> p.gs) * 4;
+  p.sc_bulk = ((K >> p.gs) % 4 == 0) ? 1 : 0;
   if (tile == 3)
     return bf16 ? launch_expert_kernel<3, 2, true, MODE, 16, 1>(p, K, L, max_items, di, stream)
                 : launch_expert_kernel<3, 2, false, MODE, 16, 1>(p, K, L, max_items, di, stream);
@@ -479,7 +481,7 @@ size_t moe_workspace_bytes(int T, int topk, int E, int H, int I) {
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
                        int T, int topk, const int32_t *qw_gu, const float *sc_gu,
                        const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
-                       void *workspace, float *y, cudaStream_t stream) {
+                       int group, void *workspace, float *y, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   const WsLayout L = ws_layout(T, topk, E, H, I);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -507,6 +509,7 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
   p.H = H;
   p.I = I;
   p.topk = topk;
+  p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
 
   p.x = x;

@@ -37,7 +37,9 @@ struct StreamParams {
   float *y;
   int ldy;
   int nstages;
-  int sc_bulk;  // 1: scales staged by bulk copy (K % 128 == 0)
+  int gs;       // log2 of the group size (5, 6 or 7)
+  int srow;     // bytes per scale row: (K / group) * 4
+  int sc_bulk;  // 1: scales staged by bulk copy (scale rows a multiple of 16 bytes)
   int fault;    // testing aid: skip the weight copies (waits then time out)
   int *status;
 };
@@ -66,9 +68,8 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
   const int K = p.K;
   const int nw = (blockDim.x >> 5) - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = K >> 5;
   const uint32_t qrow = static_cast<uint32_t>(K) >> 1;  // bytes per packed row
-  const uint32_t srow = static_cast<uint32_t>(K) >> 3;  // bytes per scale row
+  const uint32_t srow = static_cast<uint32_t>(p.srow);  // bytes per scale row
   const uint32_t qstage = RC * qrow;
   const uint32_t stage_bytes = qstage + (SCB ? RC * srow : 0u);
   const int NS = p.nstages;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     const int k0 = warp * SLICE + lane * EPL;
     const bool active = k0 < K;
     const int kc = active ? k0 : 0;  // inactive lanes read valid smem, weigh zero
-    const int g = kc >> 5;
+    const int g = kc >> p.gs;  // a lane's columns lie in one group
     uint64_t xr[MT][EPL / 2];
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
@@ -169,7 +170,10 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
         const int rows = min(RC, r1 - row0);
 #pragma unroll
         for (int r = 0; r < RC; ++r)
-          sv[r] = r < rows ? __ldg(p.sc + static_cast<size_t>(row0 + r) * G + g) : 0.f;
+          sv[r] = r < rows ? __ldg(reinterpret_cast<const float *>(
+                                     reinterpret_cast<const uint8_t *>(p.sc) +
+                                     static_cast<size_t>(row0 + r) * srow) + g)
+                           : 0.f;
       }
       int ok = 1;
       if (lane == 0) {
@@ -260,7 +264,7 @@ cudaError_t launch_tiles(const StreamParams &base, int tiles, int N, int K, int 
   const int threads = (nw + 1) * 32;
   if (nw + 1 > MAXW) return cudaErrorInvalidConfiguration;
   StreamParams p = base;
-  const size_t stage = kRowsPerChunk * (K / 2 + (SCB ? K / 8 : 0));
+  const size_t stage = kRowsPerChunk * (K / 2 + (SCB ? (K >> base.gs) * 4 : 0));
   static const int env_ns = env_int("W4A16_STREAM_NS");
   static const int env_ctas = env_int("W4A16_STREAM_CTAS");
   // MINB row blocks per SM (more when a block would exceed kMaxRowsPerCta
@@ -346,7 +350,7 @@ int stream_gemm_passes(int M, int K) {
 }
 
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
-                               const float *sc, int M, int N, int K, float *y, int ldy,
+                               const float *sc, int M, int N, int K, int group, float *y, int ldy,
                                bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   StreamParams p{};
@@ -359,7 +363,9 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
   p.K = K;
   p.y = y;
   p.ldy = ldy;
-  p.sc_bulk = (K % 128 == 0) ? 1 : 0;
+  p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
+  p.srow = (K >> p.gs) * 4;
+  p.sc_bulk = ((K >> p.gs) % 4 == 0) ? 1 : 0;
   p.status = di.status;
   p.fault = take_injected_fault() ? 1 : 0;
   const int mt = stream_tile(M, K);

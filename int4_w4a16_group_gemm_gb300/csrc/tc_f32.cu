@@ -88,6 +88,7 @@ struct FxParams {
   float *y;
   int M, N, K;
   int num_tiles;
+  int gs;  // log2 of the group size
   int *status;
 };
 
@@ -154,7 +155,9 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   const int Kw = K >> 3;
-  const int G = K >> 5;
+  const int G32 = K >> 5;       // 32-column groups (the MMA's unit)
+  const int G = K >> p.gs;       // scale groups per row
+  const int gsh = p.gs - 5;      // 32-column groups per scale group, log2
   const int nk = (K + FX_BK - 1) / FX_BK;
   const int rank = static_cast<int>(blockIdx.y);
   const int ks = static_cast<int>(gridDim.y);
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         tc_fence_after();
         const uint32_t a0 = smem_u32(smem + s * SB);
         const uint32_t b0 = a0 + FX_A_BYTES;
-        const int groups = min(2, (K >> 5) - 2 * kb);  // the last stage may hold one group
+        const int groups = min(2, G32 - 2 * kb);  // the last stage may hold one group
         bool ok = true;
         for (int h = 0; h < groups; ++h, ++g) {
           const int buf = g % FX_ACC;
@@ -348,12 +351,12 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     float acc[FX_BM];
 #pragma unroll
     for (int m = 0; m < FX_BM; ++m) acc[m] = 0.f;
-    const int g_begin = 2 * kb0, g_end = min(G, 2 * kb1);
-    float s_next = (nvalid && g_begin < g_end) ? __ldg(srow + g_begin) : 0.f;
+    const int g_begin = 2 * kb0, g_end = min(G32, 2 * kb1);
+    float s_next = (nvalid && g_begin < g_end) ? __ldg(srow + (g_begin >> gsh)) : 0.f;
     bool ok = true;
     for (int gk = g_begin, g = 0; gk < g_end; ++gk, ++g) {
-      const float s = s_next;
-      s_next = (nvalid && gk + 1 < g_end) ? __ldg(srow + gk + 1) : 0.f;
+      const float s = s_next;  // the scale of 32-column group gk
+      s_next = (nvalid && gk + 1 < g_end) ? __ldg(srow + ((gk + 1) >> gsh)) : 0.f;
       const int buf = g % FX_ACC;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], static_cast<uint32_t>(g / FX_ACC) & 1u))) {
         fail();
@@ -448,7 +451,7 @@ bool tc_f32_supported(int M, int N, int K) {
 }
 
 cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, int M, int N, int K,
-                          float *y, bool overlap, cudaStream_t stream) {
+                          int group, float *y, bool overlap, cudaStream_t stream) {
   if (!tc_f32_supported(M, N, K)) return cudaErrorInvalidValue;
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
@@ -470,6 +473,7 @@ cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, in
   p.N = N;
   p.K = K;
   p.num_tiles = (N + FX_ROWS - 1) / FX_ROWS;
+  p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
   // split K over a cluster of up to 4 CTAs so that the tiles cover the SMs
   // once (the fp32 chain of group sums is then at most 128 terms long for

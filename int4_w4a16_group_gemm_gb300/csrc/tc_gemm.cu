@@ -83,6 +83,7 @@ struct TcParams {
   float *y;
   int M, N, K;
   int tiles_m, num_tiles;
+  int gs;  // log2 of the group size
   int *status;
 };
 
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     const int row = dq / TPR, part = dq % TPR;        // weight row within the tile
     const int sub = row >> 7, rr = row & 127;
     const int Kw = K >> 3;                            // packed words per row
-    const int G = K >> 5;
+    const int G = K >> p.gs;
     // this row's byte offset inside the A region (swizzle applied per chunk)
     const uint32_t row_off =
         static_cast<uint32_t>(sub * A_SUB_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
             } else {
               w[0] = __ldg(src);
             }
-            sc[h] = __ldg(srow + (w0 >> 2));
+            sc[h] = __ldg(srow + ((w0 * 8) >> p.gs));  // a piece lies in one group
           }
         }
       };
@@ -466,7 +467,7 @@ int env_int(const char *name) {
 }  // namespace
 
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
-                           int K, float *y, bool overlap, cudaStream_t stream) {
+                           int K, int group, float *y, bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
@@ -495,6 +496,7 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   p.tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + ROWS - 1) / ROWS;
   p.num_tiles = p.tiles_m * tiles_n;
+  p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
   if (small) {
     static const int env_ks = env_int("W4A16_TC_KS");  // tuning override

@@ -57,8 +57,13 @@ def test_host_argument_checks_need_no_gpu(w4):
     # sizes
     assert lib.w4a16_gemm(fake, 0, fake, fake, 0, 1, 32, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
     assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 48, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
-    # group size other than 32
-    assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 64, 64, fake, null) == w4.W4A16_ERR_UNSUPPORTED
+    # group sizes: 32, 64 and 128 only; K a multiple of the group
+    for g in (16, 48, 256):
+        assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 256, g, fake, null) == w4.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 96, 64, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_gemm(fake, 0, fake, fake, 1, 1, 192, 128, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_gemm_launches(1, 64, 192, 64, 0, 0) >= 1
+    assert lib.w4a16_gemm_launches(1, 64, 256, 128, 1, 0) >= 1
     # bad activation dtype
     assert lib.w4a16_gemm(fake, 7, fake, fake, 1, 1, 32, 32, fake, null) == w4.W4A16_ERR_INVALID_ARG
     # misaligned operand
@@ -70,6 +75,8 @@ def test_host_argument_checks_need_no_gpu(w4):
     # quantiser
     assert lib.w4a16_quantize(null, 4, 32, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
     assert lib.w4a16_quantize(fake, 4, 40, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_quantize(fake, 4, 96, 64, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_quantize(fake, 4, 256, 16, fake, fake, null) == w4.W4A16_ERR_UNSUPPORTED
     # sort
     assert lib.w4a16_moe_sort(fake, 4, 0, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
     assert lib.w4a16_moe_sort(fake, 4, 9000, fake, fake, null) == w4.W4A16_ERR_UNSUPPORTED
@@ -79,6 +86,12 @@ def test_host_argument_checks_need_no_gpu(w4):
                               fake, max(ws - 1, 0), fake, null) == w4.W4A16_ERR_INVALID_ARG
     assert lib.w4a16_moe_gemm(fake, 1, fake, fake, 4, 2, fake, fake, fake, fake, 3, 64, 48, 32,
                               fake, ws, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    # H = 192 is not a multiple of group 128; group 16 is not taken
+    ws = w4.w4a16_moe_workspace_size(4, 2, 3, 192, 128)
+    assert lib.w4a16_moe_gemm(fake, 1, fake, fake, 4, 2, fake, fake, fake, fake, 3, 192, 128, 128,
+                              fake, ws, fake, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_gemm(fake, 1, fake, fake, 4, 2, fake, fake, fake, fake, 3, 192, 128, 16,
+                              fake, ws, fake, null) == w4.W4A16_ERR_UNSUPPORTED
 
 
 def test_workspace_size_grows_with_tokens(w4):

@@ -33,24 +33,24 @@ def w4():
     return w4
 
 
-def quantize_both(w4, w):
+def quantize_both(w4, w, group=32):
     """Device quantiser and oracle quantiser on the same W; must agree bit-exactly."""
     wd = torch.from_numpy(w).cuda()
-    qw_d, sc_d = w4.w4a16_quantize(wd)
-    qw_h, sc_h = oracle.quantize_w4a16(w)
+    qw_d, sc_d = w4.w4a16_quantize(wd, group=group)
+    qw_h, sc_h = oracle.quantize_w4a16(w, group)
     np.testing.assert_array_equal(qw_d.cpu().numpy(), qw_h)
     np.testing.assert_array_equal(sc_d.cpu().numpy().view(np.uint32), sc_h.view(np.uint32))
     return qw_d, sc_d, qw_h, sc_h
 
 
-def run_case(w4, M, N, K, dt, seed=0, outlier=0.0, algo="auto", rows=None):
+def run_case(w4, M, N, K, dt, seed=0, outlier=0.0, algo="auto", rows=None, group=32):
     x = synth.activations(seed, M, K, outlier_frac=outlier)
     w = synth.weights(seed, N, K)
-    qw_d, sc_d, qw_h, sc_h = quantize_both(w4, w)
+    qw_d, sc_d, qw_h, sc_h = quantize_both(w4, w, group)
     xt = torch.from_numpy(x)
     if dt == "bf16":
         xt = xt.to(torch.bfloat16)
-    y = w4.w4a16_gemm(xt.cuda(), qw_d, sc_d, algo=algo)
+    y = w4.w4a16_gemm(xt.cuda(), qw_d, sc_d, group=group, algo=algo)
     torch.cuda.synchronize()
     assert w4.w4a16_last_device_status() == w4.W4A16_OK
     yh = y.cpu().numpy().astype(np.float64)
@@ -58,7 +58,7 @@ def run_case(w4, M, N, K, dt, seed=0, outlier=0.0, algo="auto", rows=None):
     if rows is not None:
         xo = xo[rows]
         yh = yh[rows]
-    ref, bound = oracle.gemm_ref(xo, qw_h, sc_h)
+    ref, bound = oracle.gemm_ref(xo, qw_h, sc_h, group)
     err = np.abs(yh - ref)
     ratio = np.max(err / np.maximum(bound, 1e-300))
     assert np.all(err <= TOL[dt] * bound), f"max err/bound = {ratio:.3e}"
@@ -315,3 +315,42 @@ def test_tensor_core_overlap_back_to_back_same_output(w4, M):
     torch.cuda.synchronize()
     assert w4.w4a16_last_device_status() == w4.W4A16_OK
     assert torch.equal(y.view(torch.int32), ref_b.view(torch.int32))
+
+
+# Group sizes 64 and 128 on every kernel: the streaming kernel with scale
+# rows staged by bulk copy (K / group a multiple of 4) and loaded per lane
+# (K = 4224: 66 or 33 groups), the bf16 tensor-core kernel (whole and
+# split-K) and the fp32-exact tensor-core kernel.
+GROUP_CASES = [
+    # M, N, K, dtype, algo, outlier
+    (1, 4096, 7168, "f32", "simt", 0.0),
+    (1, 4096, 7168, "bf16", "simt", 0.0),
+    (3, 513, 4224, "f32", "simt", 0.0),
+    (2, 1000, 2048, "bf16", "simt", 0.0),
+    (64, 700, 1024, "f32", "simt", 0.01),
+    (300, 300, 7168, "bf16", "tc", 0.0),
+    (64, 4096, 7168, "bf16", "tc", 0.01),
+    (31, 40, 4224, "bf16", "tc", 0.0),
+    (64, 4096, 7168, "f32", "tc", 0.01),
+    (17, 1000, 4224, "f32", "tc", 0.0),
+    (33, 300, 384, "f32", "tc", 0.0),
+]
+
+
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("M,N,K,dt,algo,outlier", GROUP_CASES)
+def test_group_sizes_64_and_128(w4, group, M, N, K, dt, algo, outlier):
+    _, ratio = run_case(w4, M, N, K, dt, seed=M + N + K + group, outlier=outlier, algo=algo,
+                        group=group)
+    if dt == "f32":
+        assert ratio < 0.1
+
+
+def test_group_size_mismatch_is_rejected(w4):
+    x = torch.zeros((1, 192), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((8, 24), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((8, 3), dtype=torch.float32, device="cuda")
+    for group, code in ((128, w4.W4A16_ERR_INVALID_ARG), (16, w4.W4A16_ERR_UNSUPPORTED)):
+        with pytest.raises(w4.W4A16Error) as ei:
+            w4.w4a16_gemm(x, qw, sc, group=group)
+        assert ei.value.code == code

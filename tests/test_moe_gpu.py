@@ -55,26 +55,26 @@ def test_sort_skewed_and_invalid(w4):
     assert w4.w4a16_last_device_status() == w4.W4A16_OK  # cleared by the read
 
 
-def build_experts_host(seed, E, H, I):
+def build_experts_host(seed, E, H, I, group=32):
     qgu, sgu, qdn, sdn = [], [], [], []
     for e in range(E):
-        a, b = oracle.quantize_w4a16(synth.weights(seed, 2 * I, H, sub=2 * e))
-        c, d = oracle.quantize_w4a16(synth.weights(seed, H, I, sub=2 * e + 1))
+        a, b = oracle.quantize_w4a16(synth.weights(seed, 2 * I, H, sub=2 * e), group)
+        c, d = oracle.quantize_w4a16(synth.weights(seed, H, I, sub=2 * e + 1), group)
         qgu.append(a); sgu.append(b); qdn.append(c); sdn.append(d)
     return np.stack(qgu), np.stack(sgu), np.stack(qdn), np.stack(sdn)
 
 
-def check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16):
+def check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16, group=32):
     xt = torch.from_numpy(x)
     if bf16:
         xt = xt.to(torch.bfloat16)
     dev = [torch.from_numpy(a).cuda() for a in (qgu, sgu, qdn, sdn)]
     y = w4.w4a16_moe_gemm(xt.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(rw).cuda(),
-                          *dev)
+                          *dev, group=group)
     torch.cuda.synchronize()
     assert w4.w4a16_last_device_status() == w4.W4A16_OK
     ref, tol = oracle.moe_ref(xt.float().numpy(), ids, rw, qgu, sgu, qdn, sdn, bf16,
-                              eps=4e-3 if bf16 else 1e-5)
+                              eps=4e-3 if bf16 else 1e-5, group=group)
     err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= tol), f"max err/tol = {np.max(err / tol):.3e}"
     return y
@@ -89,6 +89,19 @@ def test_small_moe(w4, bf16, T, H, I, E, topk):
     ids, rw = synth.routing(seed, T, topk, E)
     qgu, sgu, qdn, sdn = build_experts_host(seed, E, H, I)
     check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("T,H,I,E,topk", [(5, 256, 128, 6, 2), (16, 1024, 384, 9, 4)])
+def test_small_moe_group_sizes(w4, bf16, group, T, H, I, E, topk):
+    """Groups of 64 and 128 on both expert GEMMs; I = 384 with group 128
+    gives 3 scales per down-projection row (loaded per lane, not staged)."""
+    seed = T + H + E + group
+    x = synth.activations(seed, T, H)
+    ids, rw = synth.routing(seed, T, topk, E)
+    qgu, sgu, qdn, sdn = build_experts_host(seed, E, H, I, group)
+    check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16, group)
 
 
 def test_moe_many_tokens_one_expert(w4):

@@ -205,6 +205,76 @@ def test_quantizer_groups_are_independent():
     np.testing.assert_array_equal(qw[:, 12:], qw2[:, 12:])
 
 
+def brute_quantize(w, group):
+    """Scalar quantiser on Python numbers, one group at a time -> (nibbles, scales).
+
+    s = fp32(max|w| / 7) (a double quotient rounded once more to fp32 is the
+    correctly rounded fp32 quotient), q = round-half-even(fp32(w / s))
+    clamped to [-8, 7], q = 0 where s = 0."""
+    N, K = w.shape
+    nib = [[0] * K for _ in range(N)]
+    scales = [[0.0] * (K // group) for _ in range(N)]
+    for n in range(N):
+        for g in range(K // group):
+            vals = [float(w[n, g * group + j]) for j in range(group)]
+            s = f32(max(abs(v) for v in vals) / 7.0)
+            scales[n][g] = s
+            for j, v in enumerate(vals):
+                q = 0 if s == 0.0 else max(-8, min(7, round(f32(v / s))))
+                nib[n][g * group + j] = q + 8
+    return nib, scales
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_quantizer_against_scalar_loop_all_group_sizes(group):
+    N, K = 3, 384
+    w = synth.weights(11, N, K)
+    w[1, group:2 * group] = 0.0                       # an all-zero group
+    w[2, 5] = np.float32(40.0)                        # one outlier sets its group's scale
+    qw, sc = oracle.quantize_w4a16(w, group)
+    assert qw.shape == (N, K // 8) and sc.shape == (N, K // group)
+    nib, scales = brute_quantize(w, group)
+    for n in range(N):
+        for k in range(K):
+            assert word_nibble(int(qw[n, k // 8]), k % 8) == nib[n][k], (n, k)
+        for g in range(K // group):
+            assert float(sc[n, g]) == scales[n][g], (n, g)
+    assert sc[1, 1] == 0.0
+    assert sc[2, 0] == np.float32(f32(40.0 / 7.0))
+    # a group of 64 or 128 shares one scale where groups of 32 would not
+    if group > 32:
+        q32, s32 = oracle.quantize_w4a16(w, 32)
+        assert not np.array_equal(np.repeat(sc, group // 32, axis=1), s32)
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_quantizer_groups_are_independent_larger_groups(group):
+    w = synth.weights(12, 4, 512)
+    qw, sc = oracle.quantize_w4a16(w, group)
+    w2 = w.copy()
+    w2[:, group:2 * group] *= np.float32(100.0)       # change group 1 only
+    qw2, sc2 = oracle.quantize_w4a16(w2, group)
+    keep = np.ones(512 // group, bool)
+    keep[1] = False
+    np.testing.assert_array_equal(sc[:, keep], sc2[:, keep])
+    wpg = group // 8                                  # packed words per group
+    np.testing.assert_array_equal(qw[:, :wpg], qw2[:, :wpg])
+    np.testing.assert_array_equal(qw[:, 2 * wpg:], qw2[:, 2 * wpg:])
+    assert np.all(sc2[:, 1] > 50 * sc[:, 1])           # the changed group's scale follows
+
+
+def test_dequant_larger_group_uses_one_scale_per_group():
+    N, K = 2, 256
+    qw = oracle.pack_nibbles(np.tile(np.arange(16, dtype=np.uint8), (N, K // 16)))
+    for group in (64, 128):
+        sc = (np.arange(N * (K // group), dtype=np.float32).reshape(N, K // group) + 1) * 0.25
+        got = oracle.dequantize(qw, sc, group)
+        ref = brute_dequant(qw, sc, group)
+        np.testing.assert_array_equal(got, np.array(ref, np.float32))
+        # column k of row n is (k % 16 - 8) * sc[n][k // group]
+        assert got[1, group] == np.float32((group % 16 - 8) * sc[1, 1])
+
+
 # ------------------------------------------------------------ GEMM
 def brute_gemm(x, qw, sc, group=32):
     """Exact rational triple loop: y[m][n] = sum_k x[m][k] * W_hat[n][k]."""
@@ -240,6 +310,19 @@ def test_gemm_matches_exact_triple_loop(M, N, K):
             assert bound[m, n] == pytest.approx(float(be[m][n]), rel=1e-13)
     # a transposed operand would not even have this shape
     assert y.shape == (M, N)
+
+
+@pytest.mark.parametrize("M,N,K,group", [(2, 3, 128, 64), (1, 2, 256, 128), (3, 2, 384, 128)])
+def test_gemm_matches_exact_triple_loop_larger_groups(M, N, K, group):
+    x = synth.activations(8, M, K)
+    w = synth.weights(8, N, K)
+    qw, sc = oracle.quantize_w4a16(w, group)
+    y, bound = oracle.gemm_ref(x, qw, sc, group)
+    ye, be = brute_gemm(x, qw, sc, group)
+    for m in range(M):
+        for n in range(N):
+            assert abs(y[m, n] - float(ye[m][n])) <= K * 2.0 ** -52 * float(be[m][n])
+            assert bound[m, n] == pytest.approx(float(be[m][n]), rel=1e-13)
 
 
 def test_gemm_one_hot_reproduces_columns():

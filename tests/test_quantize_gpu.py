@@ -20,9 +20,9 @@ def w4():
     return w4
 
 
-def check(w4, w):
-    qw_d, sc_d = w4.w4a16_quantize(torch.from_numpy(w).cuda())
-    qw_h, sc_h = oracle.quantize_w4a16(w)
+def check(w4, w, group=32):
+    qw_d, sc_d = w4.w4a16_quantize(torch.from_numpy(w).cuda(), group=group)
+    qw_h, sc_h = oracle.quantize_w4a16(w, group)
     np.testing.assert_array_equal(qw_d.cpu().numpy(), qw_h)
     np.testing.assert_array_equal(sc_d.cpu().numpy().view(np.uint32), sc_h.view(np.uint32))
 
@@ -53,3 +53,12 @@ def test_quantizer_matches_random_mixed_scales(w4):
     w = synth.weights(5, 256, 1024)
     w *= np.float32(10.0) ** np.random.default_rng(0).uniform(-6, 6, size=(256, 1)).astype(np.float32)
     check(w4, w.astype(np.float32))
+
+
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("N,K", [(1, 128), (3, 384), (512, 1024), (4096, 7168), (7, 4224)])
+def test_quantizer_group_sizes(w4, group, N, K):
+    w = synth.weights(N + K + group, N, K)
+    w[0, :group] = 0.0                                # an all-zero group
+    w[-1, (group + 3) % K] = np.float32(-25.0)        # an outlier owning a group's scale
+    check(w4, w, group)
