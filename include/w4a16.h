@@ -107,17 +107,23 @@ enum {
    * launched just before does not write qw or sc (true when weights are
    * prepared earlier, as in a decode loop). Every kernel honours it: the
    * tensor-core kernels dequantise their first stages of weights early. */
-  W4A16_FLAG_OVERLAP = 1u
+  W4A16_FLAG_OVERLAP = 1u,
+  /* bf16 output: y is [M][N] bf16 (16-bit elements) instead of fp32; each
+   * element is the fp32 result the same call would write without the flag,
+   * rounded to nearest (ties to even). Halves the output bytes for callers
+   * whose next layer consumes bf16. */
+  W4A16_FLAG_OUT_BF16 = 2u
 };
 
 /* w4a16_gemm with an explicit kernel choice and launch flags (0 = none);
  * W4A16_ALGO_TC takes bf16 activations, or fp32 activations with M <= 64
- * and K <= 16384 (UNSUPPORTED otherwise). Same arguments and errors as
- * w4a16_gemm, plus INVALID_ARG for unknown flags. */
+ * and K <= 16384 (UNSUPPORTED otherwise). y is fp32 [M][N], or bf16
+ * [M][N] with W4A16_FLAG_OUT_BF16 (16-byte aligned either way). Same
+ * arguments and errors as w4a16_gemm, plus INVALID_ARG for unknown flags. */
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt,
                            const int32_t *qw, const float *sc,
                            int M, int N, int K, int group,
-                           float *y, w4a16_algo algo, unsigned int flags,
+                           void *y, w4a16_algo algo, unsigned int flags,
                            w4a16_stream_t stream);
 
 /* Number of kernel launches a w4a16_gemm_ex call with these arguments makes

@@ -6,7 +6,8 @@ and streams. There is no fallback: if the shared library is missing or
 fails to load, importing this package raises.
 
 Functions keep the C names:
-    w4a16_gemm(x, qw, sc, y=None, group=32, algo="auto", stream=None) -> y
+    w4a16_gemm(x, qw, sc, y=None, group=32, algo="auto", overlap=False,
+               stream=None, out_dtype="f32") -> y
     w4a16_quantize(w, group=32, stream=None) -> (qw, sc)
     w4a16_moe_sort(expert_ids, E, stream=None) -> (offsets, perm)
     w4a16_moe_workspace_size(T, topk, E, H, I) -> int
@@ -36,6 +37,7 @@ ACT_BF16 = 1
 
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 FLAG_OVERLAP = 1
+FLAG_OUT_BF16 = 2
 
 # name -> (restype, argtypes), mirroring include/w4a16.h
 _VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -120,12 +122,13 @@ def _need(t, dtype, name):
 
 
 def w4a16_gemm(x, qw, sc, y=None, group: int = 32, algo: str = "auto", overlap: bool = False,
-               stream=None):
+               stream=None, out_dtype: str = "f32"):
     """y[M, N] = x[M, K] @ W_hat[N, K]^T via the C ABI.
 
     overlap=True sets W4A16_FLAG_OVERLAP: the weight stream may start while
     the previous kernel on the stream is still running (the caller promises
-    that kernel does not write qw or sc)."""
+    that kernel does not write qw or sc). out_dtype="bf16" sets
+    W4A16_FLAG_OUT_BF16: y is bf16, the fp32 result rounded to nearest even."""
     import torch
     xdt = _act_dtype(x)
     _need(x, x.dtype, "x")
@@ -133,11 +136,15 @@ def w4a16_gemm(x, qw, sc, y=None, group: int = 32, algo: str = "auto", overlap: 
     _need(sc, torch.float32, "sc")
     M, K = x.shape
     N = qw.shape[0]
+    if out_dtype not in ("f32", "bf16"):
+        raise ValueError("out_dtype must be 'f32' or 'bf16'")
+    ydt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    _need(y, torch.float32, "y")
+        y = torch.empty((M, N), dtype=ydt, device=x.device)
+    _need(y, ydt, "y")
+    flags = (FLAG_OVERLAP if overlap else 0) | (FLAG_OUT_BF16 if out_dtype == "bf16" else 0)
     code = lib.w4a16_gemm_ex(_ptr(x), xdt, _ptr(qw), _ptr(sc), M, N, K, group, _ptr(y),
-                             ALGOS[algo], FLAG_OVERLAP if overlap else 0, _stream_handle(stream))
+                             ALGOS[algo], flags, _stream_handle(stream))
     _check("w4a16_gemm", code)
     return y
 

@@ -121,10 +121,11 @@ int w4a16_gemm_launches(int M, int N, int K, int group, w4a16_act_dtype xdt, w4a
 }
 
 w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw,
-                           const float *sc, int M, int N, int K, int group, float *y,
+                           const float *sc, int M, int N, int K, int group, void *y,
                            w4a16_algo algo, unsigned int flags, w4a16_stream_t stream) {
   if (!x || !qw || !sc || !y) return W4A16_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned int>(W4A16_FLAG_OVERLAP)) return W4A16_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned int>(W4A16_FLAG_OVERLAP | W4A16_FLAG_OUT_BF16))
+    return W4A16_ERR_INVALID_ARG;
   GemmKernel kind;
   const w4a16_status st = plan_gemm(M, N, K, group, xdt, algo, &kind);
   if (st != W4A16_OK) return st;
@@ -133,14 +134,16 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
   if (!device_ready()) return W4A16_ERR_CUDA;
   const bool bf16 = xdt == W4A16_ACT_BF16;
   const bool overlap = (flags & W4A16_FLAG_OVERLAP) != 0;
+  const bool ybf16 = (flags & W4A16_FLAG_OUT_BF16) != 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kind == GemmKernel::TensorBf16)
-    return from_cuda(
-        launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, group, y, overlap, s));
+    return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, group, y,
+                                    ybf16, overlap, s));
   if (kind == GemmKernel::TensorF32)
-    return from_cuda(
-        launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, group, y, overlap, s));
-  return from_cuda(launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, group, y, N, overlap, s));
+    return from_cuda(launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, group, y,
+                                   ybf16, overlap, s));
+  return from_cuda(
+      launch_stream_gemm(x, bf16, K, qw, sc, M, N, K, group, y, ybf16, N, overlap, s));
 }
 
 w4a16_status w4a16_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *qw, const float *sc,

@@ -2,6 +2,7 @@
 // mbarrier waits, bulk (TMA) copies and small conversions. sm_103a only.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -134,6 +135,15 @@ __device__ __forceinline__ void griddep_wait() {
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Store element i of the output: fp32, or rounded to bf16 (to nearest,
+// ties to even) when `bf16` is set and y holds 16-bit elements.
+__device__ __forceinline__ void store_y(void *y, size_t i, float v, int bf16) {
+  if (bf16)
+    static_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float *>(y)[i] = v;
 }
 
 // ---------------------------------------------------------------- numbers

@@ -27,12 +27,13 @@ bool take_injected_fault();
 // ------------------------------------------------------------ streaming kernel
 // y = x * W_hat^T on CUDA cores for any M >= 1 (K % 32 == 0, K <= 16384),
 // in one launch: a 2-D grid of row blocks x token tiles of up to 3 tokens.
-// `ldx`/`ldy` are row strides in elements. `overlap` launches with
+// `ldx`/`ldy` are row strides in elements. y is fp32, or bf16 (rounded to
+// nearest even from the fp32 sum) when `y_bf16`. `overlap` launches with
 // programmatic stream serialisation: the weight stream may start before the
 // previous kernel on the stream has finished (x and y stay ordered).
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
-                               const float *sc, int M, int N, int K, int group, float *y,
-                               int ldy, bool overlap, cudaStream_t stream);
+                               const float *sc, int M, int N, int K, int group, void *y,
+                               bool y_bf16, int ldy, bool overlap, cudaStream_t stream);
 // Largest K the streaming kernel accepts for a token tile of `mt` (1, 2, 3).
 int max_k_stream(int mt);
 // Token tile width the streaming kernel uses for M tokens.
@@ -43,15 +44,17 @@ int stream_gemm_passes(int M, int K);
 
 // ------------------------------------------------------------ tensor-core kernel
 // Same contract for bf16 activations on tcgen05 tensor cores, including
-// `overlap`.
+// `y_bf16` and `overlap`.
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M,
-                           int N, int K, int group, float *y, bool overlap, cudaStream_t stream);
+                           int N, int K, int group, void *y, bool y_bf16, bool overlap,
+                           cudaStream_t stream);
 bool tc_gemm_supported(int M, int N, int K);
 // fp32 activations on the tensor cores, exact to fp32 accumulation: each
 // activation is split into three bf16 pieces and the group scales are
 // applied in fp32 outside the MMA (M <= 64).
 cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, int M, int N,
-                          int K, int group, float *y, bool overlap, cudaStream_t stream);
+                          int K, int group, void *y, bool y_bf16, bool overlap,
+                          cudaStream_t stream);
 bool tc_f32_supported(int M, int N, int K);
 
 // ------------------------------------------------------------ quantiser

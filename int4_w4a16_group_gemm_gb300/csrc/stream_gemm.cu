@@ -34,7 +34,8 @@ struct StreamParams {
   const int32_t *qw;
   const float *sc;
   int N, K;
-  float *y;
+  void *y;      // fp32, or bf16 when ybf16
+  int ybf16;
   int ldy;
   int nstages;
   int gs;       // log2 of the group size (5, 6 or 7)
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     const float *v = red + static_cast<size_t>(i) * nw;
     float a = 0.f;
     for (int w = 0; w < nw; ++w) a += v[w];
-    p.y[static_cast<size_t>(m0 + t) * p.ldy + r0 + row] = a;
+    store_y(p.y, static_cast<size_t>(m0 + t) * p.ldy + r0 + row, a, p.ybf16);
   }
 }
 
@@ -306,7 +307,8 @@ cudaError_t launch_tiles(const StreamParams &base, int tiles, int N, int K, int 
                                            static_cast<size_t>(t0) * MT * p.ldx)
                : static_cast<const void *>(static_cast<const float *>(p.x) +
                                            static_cast<size_t>(t0) * MT * p.ldx);
-    q.y = p.y + static_cast<size_t>(t0) * MT * p.ldy;
+    q.y = static_cast<uint8_t *>(p.y) +
+          static_cast<size_t>(t0) * MT * p.ldy * (p.ybf16 ? 2 : 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, nt);
     cfg.blockDim = dim3(threads);
@@ -350,7 +352,7 @@ int stream_gemm_passes(int M, int K) {
 }
 
 cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_t *qw,
-                               const float *sc, int M, int N, int K, int group, float *y, int ldy,
+                               const float *sc, int M, int N, int K, int group, void *y, bool y_bf16, int ldy,
                                bool overlap, cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   StreamParams p{};
@@ -362,6 +364,7 @@ cudaError_t launch_stream_gemm(const void *x, bool x_bf16, int ldx, const int32_
   p.N = N;
   p.K = K;
   p.y = y;
+  p.ybf16 = y_bf16 ? 1 : 0;
   p.ldy = ldy;
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.srow = (K >> p.gs) * 4;

@@ -85,7 +85,8 @@ constexpr uint32_t FX_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
 struct FxParams {
   const int32_t *qw;
   const float *sc;
-  float *y;
+  void *y;  // fp32, or bf16 when ybf16
+  int ybf16;
   int M, N, K;
   int num_tiles;
   int gs;  // log2 of the group size
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         const int col = (m + nl) & (FX_BM - 1);
         float v = recv[i * FX_BM + col];
         for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * FX_BM + col];
-        p.y[static_cast<size_t>(m) * p.N + n0 + nl] = v;
+        store_y(p.y, static_cast<size_t>(m) * p.N + n0 + nl, v, p.ybf16);
       }
     }
     // no CTA leaves while its shared memory may still be copied from
@@ -451,7 +452,7 @@ bool tc_f32_supported(int M, int N, int K) {
 }
 
 cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, int M, int N, int K,
-                          int group, float *y, bool overlap, cudaStream_t stream) {
+                          int group, void *y, bool y_bf16, bool overlap, cudaStream_t stream) {
   if (!tc_f32_supported(M, N, K)) return cudaErrorInvalidValue;
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
@@ -469,6 +470,7 @@ cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, in
   p.qw = qw;
   p.sc = sc;
   p.y = y;
+  p.ybf16 = y_bf16 ? 1 : 0;
   p.M = M;
   p.N = N;
   p.K = K;

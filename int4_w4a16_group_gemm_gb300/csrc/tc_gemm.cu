@@ -80,7 +80,8 @@ struct TcCfg {
 struct TcParams {
   const int32_t *qw;
   const float *sc;
-  float *y;
+  void *y;  // fp32, or bf16 when ybf16
+  int ybf16;
   int M, N, K;
   int tiles_m, num_tiles;
   int gs;  // log2 of the group size
@@ -368,7 +369,9 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
             if (ne < p.N) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (mb + j < p.M) p.y[static_cast<size_t>(mb + j) * p.N + ne] = __uint_as_float(r[j]);
+                if (mb + j < p.M)
+                  store_y(p.y, static_cast<size_t>(mb + j) * p.N + ne, __uint_as_float(r[j]),
+                          p.ybf16);
             }
           }
         }
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         const int col = (m + nl) & (BM - 1);
         float v = recv[i * BM + col];
         for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * BM + col];
-        p.y[static_cast<size_t>(m0 + m) * p.N + n0 + nl] = v;
+        store_y(p.y, static_cast<size_t>(m0 + m) * p.N + n0 + nl, v, p.ybf16);
       }
     }
     // no CTA leaves while its shared memory may still be copied from
@@ -467,7 +470,8 @@ int env_int(const char *name) {
 }  // namespace
 
 cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
-                           int K, int group, float *y, bool overlap, cudaStream_t stream) {
+                           int K, int group, void *y, bool y_bf16, bool overlap,
+                           cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
@@ -490,6 +494,7 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   p.qw = qw;
   p.sc = sc;
   p.y = y;
+  p.ybf16 = y_bf16 ? 1 : 0;
   p.M = M;
   p.N = N;
   p.K = K;

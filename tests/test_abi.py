@@ -71,7 +71,9 @@ def test_host_argument_checks_need_no_gpu(w4):
     # bad algo
     assert lib.w4a16_gemm_ex(fake, 0, fake, fake, 1, 1, 32, 32, fake, 9, 0, null) == w4.W4A16_ERR_INVALID_ARG
     # unknown launch flag
-    assert lib.w4a16_gemm_ex(fake, 0, fake, fake, 1, 1, 32, 32, fake, 0, 2, null) == w4.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_gemm_ex(fake, 0, fake, fake, 1, 1, 32, 32, fake, 0, 4, null) == w4.W4A16_ERR_INVALID_ARG
+    # the bf16-output flag is known: the call gets as far as the alignment check
+    assert lib.w4a16_gemm_ex(fake, 0, fake, fake, 1, 1, 32, 32, odd, 0, 2, null) == w4.W4A16_ERR_ALIGNMENT
     # quantiser
     assert lib.w4a16_quantize(null, 4, 32, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG
     assert lib.w4a16_quantize(fake, 4, 40, 32, fake, fake, null) == w4.W4A16_ERR_INVALID_ARG

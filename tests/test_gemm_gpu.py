@@ -354,3 +354,48 @@ def test_group_size_mismatch_is_rejected(w4):
         with pytest.raises(w4.W4A16Error) as ei:
             w4.w4a16_gemm(x, qw, sc, group=group)
         assert ei.value.code == code
+
+
+# bf16 output (W4A16_FLAG_OUT_BF16) on every kernel: each element is the
+# fp32 result of the same call rounded to nearest even, and within the
+# tolerance plus one bf16 rounding (2^-8 |y|) of the oracle.
+OUT_BF16_CASES = [
+    # M, N, K, x dtype, algo, group
+    (1, 4096, 7168, "f32", "simt", 32),
+    (3, 513, 4224, "bf16", "simt", 64),
+    (7, 300, 1024, "f32", "simt", 128),
+    (300, 300, 7168, "bf16", "tc", 32),
+    (64, 4096, 7168, "bf16", "tc", 128),
+    (64, 4096, 7168, "f32", "tc", 32),
+    (17, 1000, 4224, "f32", "tc", 64),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dt,algo,group", OUT_BF16_CASES)
+def test_bf16_output(w4, M, N, K, dt, algo, group):
+    seed = 3 * M + N + K
+    x = synth.activations(seed, M, K)
+    w = synth.weights(seed, N, K)
+    qw_d, sc_d, qw_h, sc_h = quantize_both(w4, w, group)
+    xt = torch.from_numpy(x)
+    if dt == "bf16":
+        xt = xt.to(torch.bfloat16)
+    xd = xt.cuda()
+    y32 = w4.w4a16_gemm(xd, qw_d, sc_d, group=group, algo=algo)
+    y16 = w4.w4a16_gemm(xd, qw_d, sc_d, group=group, algo=algo, out_dtype="bf16")
+    torch.cuda.synchronize()
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    assert y16.dtype == torch.bfloat16 and y16.shape == (M, N)
+    # same fp32 sums, then one round-to-nearest-even (torch's conversion)
+    assert torch.equal(y16.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+    ref, bound = oracle.gemm_ref(xt.float().numpy(), qw_h, sc_h, group)
+    err = np.abs(y16.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= TOL[dt] * bound * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref))
+
+
+def test_bf16_output_needs_a_bf16_buffer(w4):
+    x = torch.zeros((1, 64), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((8, 8), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((8, 2), dtype=torch.float32, device="cuda")
+    with pytest.raises(TypeError):
+        w4.w4a16_gemm(x, qw, sc, y=torch.zeros((1, 8), device="cuda"), out_dtype="bf16")
