@@ -39,6 +39,17 @@ Readings where the pages are silent (each is listed in the design notes):
     GEMM consumes), y[t] = sum over the token's k slots, in slot order, of
     route_w * (h @ W_down^T).
 
+  * MoE routing (the "DeepSeekV3/Kimi-style ... MoE routing with shared
+    expert" of [QC] "The Context: A Native DDTree Engine Takes Shape" and
+    [PC] "The Context: Phase 3 of a Custom Inference Stack"; the pages give
+    no formula, so the published DeepSeek-V3 gate is taken): fp32 router
+    logits l = x @ W_r^T, scores s = sigmoid(l), the k experts with the
+    largest s + b (b an optional per-expert selection bias; equal values go
+    to the lower expert id), weights s_j / sum of the k chosen s times a
+    routing scale;
+  * shared expert: a SwiGLU expert that every token uses with weight 1,
+    added after the routed slots.
+
 Every function is pinned by tests against closed forms, brute force and
 invariants (tests/test_oracle_pins.py); none is "parity unpinned".
 """
@@ -254,3 +265,80 @@ def moe_ref(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, bf16_mode: bool,
         # the fp32 routing-weight product and the fp32 slot sum
         tol[t] += (topk + 2) * 2.0 ** -24 * absacc
     return y, tol
+
+
+def sigmoid(v: np.ndarray) -> np.ndarray:
+    """Logistic function 1 / (1 + exp(-v)) in fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def moe_route_ref(x, router_w, bias, topk: int, route_scale: float):
+    """Router of the MoE block: logits, top-k expert ids and routing weights.
+
+    [QC] "The Context: A Native DDTree Engine Takes Shape" and [PC] "The
+    Context: Phase 3 of a Custom Inference Stack" (DeepSeekV3/Kimi-style MoE
+    routing); the gate itself is the published DeepSeek-V3 one:
+        l[t, e]  = x[t] . W_r[e]                      (x as given, fp32 values)
+        s[t, e]  = sigmoid(l[t, e])
+        ids[t]   = the topk experts with the largest s + b, in decreasing
+                   order of s + b; equal values go to the lower expert id
+        w[t, j]  = route_scale * s[t, ids[t, j]] / sum_j' s[t, ids[t, j']]
+    ``bias`` may be None (all zero). Returns (logits, bound, ids, w):
+    logits and bound = |x| @ |W_r|^T in fp64, ids int32 [T, topk], w fp64.
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    wr = np.asarray(router_w, dtype=np.float32).astype(np.float64)
+    T = x64.shape[0]
+    E = wr.shape[0]
+    if not 1 <= topk <= E:
+        raise ValueError("topk must be in 1..E")
+    logits = x64 @ wr.T
+    bound = np.abs(x64) @ np.abs(wr).T
+    s = sigmoid(logits)
+    b = np.zeros(E) if bias is None else np.asarray(bias, dtype=np.float32).astype(np.float64)
+    sel = s + b
+    ids = np.zeros((T, topk), dtype=np.int32)
+    w = np.zeros((T, topk), dtype=np.float64)
+    for t in range(T):
+        # a stable sort on -sel keeps equal values in increasing expert id
+        order = np.argsort(-sel[t], kind="stable")[:topk]
+        ids[t] = order
+        w[t] = route_scale * s[t, order] / np.sum(s[t, order])
+    return logits, bound, ids, w
+
+
+class _ExpertsWithShared:
+    """Expert tensors indexable by id: the routed ones, then the shared one at id E."""
+
+    def __init__(self, routed, shared, E):
+        self.routed, self.shared, self.E = routed, shared, E
+
+    def __getitem__(self, e):
+        return self.shared if e == self.E else self.routed[e]
+
+
+def moe_block_ref(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, shared, bf16_mode: bool,
+                  eps: float, group: int = GROUP, tokens=None):
+    """MoE block: the routed layer of ``moe_ref`` plus the shared expert.
+
+    [QC] "The Context: A Native DDTree Engine Takes Shape" and "The INT4
+    Milestone" (MoE routing with a shared expert; routed and shared experts
+    run through the INT4 path). ``shared`` is (qw_gu_s, sc_gu_s, qw_dn_s,
+    sc_dn_s) of one SwiGLU expert (its width may differ from the routed
+    experts'), or None. The shared expert is an extra slot after the routed
+    ones, used by every token with weight 1:
+        y[t] = sum_j w[t, j] * expert_{ids[t, j]}(x[t]) + expert_shared(x[t]).
+    Returns (y, tol) as ``moe_ref``.
+    """
+    if shared is None:
+        return moe_ref(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, bf16_mode, eps,
+                       group, tokens)
+    ids = np.asarray(expert_ids)
+    T, topk = ids.shape
+    E = len(qw_gu) if not isinstance(qw_gu, dict) else max(qw_gu) + 1
+    E = max(E, int(ids.max()) + 1)
+    ids_ext = np.concatenate([ids, np.full((T, 1), E, dtype=ids.dtype)], axis=1)
+    w_ext = np.concatenate([np.asarray(route_w, dtype=np.float64), np.ones((T, 1))], axis=1)
+    m = [_ExpertsWithShared(a, b, E) for a, b in zip((qw_gu, sc_gu, qw_dn, sc_dn), shared)]
+    return moe_ref(x, ids_ext, w_ext, m[0], m[1], m[2], m[3], bf16_mode, eps, group, tokens)

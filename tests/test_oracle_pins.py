@@ -491,3 +491,99 @@ def test_moe_ref_token_permutation_and_slot_order():
     sub, _ = oracle.moe_ref(x, ids, rw, qgu, sgu, qdn, sdn, False, eps=1e-5, tokens=[1, 3])
     np.testing.assert_array_equal(sub[[1, 3]], y[[1, 3]])
     assert not sub[[0, 2, 4]].any()
+
+
+# ------------------------------------------------------------ MoE routing and block
+def brute_route(x, wr, bias, topk, scale):
+    """Pure-Python routing: exact rational logits, math.exp sigmoid, sort by key."""
+    T, H = x.shape
+    E = wr.shape[0]
+    logits, ids, ws = [], [], []
+    for t in range(T):
+        lt = [float(sum(Fraction(float(x[t, h])) * Fraction(float(wr[e, h])) for h in range(H)))
+              for e in range(E)]
+        s = [1.0 / (1.0 + math.exp(-v)) for v in lt]
+        b = [0.0] * E if bias is None else [float(v) for v in bias]
+        order = sorted(range(E), key=lambda e: (-(s[e] + b[e]), e))[:topk]
+        tot = math.fsum(s[e] for e in order)
+        logits.append(lt)
+        ids.append(order)
+        ws.append([scale * s[e] / tot for e in order])
+    return logits, ids, ws
+
+
+@pytest.mark.parametrize("T,E,H,topk,use_bias", [(4, 7, 16, 3, False), (3, 12, 32, 5, True),
+                                                 (2, 5, 8, 5, False)])
+def test_route_against_brute_force(T, E, H, topk, use_bias):
+    x = synth.activations(21, T, H)
+    wr = synth.weights(21, E, H)
+    bias = (synth.weights(22, 1, E)[0] * np.float32(0.1)) if use_bias else None
+    logits, bound, ids, w = oracle.moe_route_ref(x, wr, bias, topk, 2.5)
+    bl, bi, bw = brute_route(x, wr, bias, topk, 2.5)
+    np.testing.assert_array_equal(ids, np.array(bi))
+    np.testing.assert_allclose(logits, np.array(bl), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(w, np.array(bw), rtol=1e-13, atol=0)
+    assert np.all(bound >= np.abs(logits))
+    np.testing.assert_allclose(w.sum(axis=1), 2.5, rtol=1e-14)      # weights sum to the scale
+
+
+def test_route_ties_bias_and_full_selection():
+    H = 8
+    x = np.ones((1, H), np.float32)
+    wr = np.zeros((6, H), np.float32)
+    wr[1] = wr[4] = 0.25                      # experts 1 and 4: equal logits 2.0
+    wr[2] = -0.5                              # expert 2: logit -4
+    _, _, ids, w = oracle.moe_route_ref(x, wr, None, 2, 1.0)
+    assert list(ids[0]) == [1, 4]             # the tie goes to the lower id first
+    np.testing.assert_allclose(w[0], [0.5, 0.5], rtol=1e-15)
+    # a large bias forces expert 2 in; its weight still uses the plain sigmoid
+    bias = np.zeros(6, np.float32)
+    bias[2] = 10.0
+    _, _, ids, w = oracle.moe_route_ref(x, wr, bias, 2, 1.0)
+    assert list(ids[0]) == [2, 1]
+    s2, s1 = 1 / (1 + math.exp(4.0)), 1 / (1 + math.exp(-2.0))
+    np.testing.assert_allclose(w[0], [s2 / (s1 + s2), s1 / (s1 + s2)], rtol=1e-14)
+    # topk = E: every expert, in decreasing score order, ties by id
+    _, _, ids, w = oracle.moe_route_ref(x, wr, None, 6, 3.0)
+    assert list(ids[0]) == [1, 4, 0, 3, 5, 2]
+    s = np.array([0.5, s1, s2, 0.5, s1, 0.5])
+    np.testing.assert_allclose(w[0], 3.0 * s[[1, 4, 0, 3, 5, 2]] / s.sum(), rtol=1e-14)
+
+
+def _small_experts(seed, E, H, I, group=32):
+    out = [[], [], [], []]
+    for e in range(E):
+        a, b = oracle.quantize_w4a16(synth.weights(seed, 2 * I, H, sub=2 * e), group)
+        c, d = oracle.quantize_w4a16(synth.weights(seed, H, I, sub=2 * e + 1), group)
+        for lst, v in zip(out, (a, b, c, d)):
+            lst.append(v)
+    return [np.stack(v) for v in out]
+
+
+def test_moe_block_shared_expert_closed_forms():
+    T, H, I, Is, E, topk = 3, 64, 32, 64, 4, 2
+    x = synth.activations(31, T, H)
+    ids, rw = synth.routing(31, T, topk, E)
+    qgu, sgu, qdn, sdn = _small_experts(31, E, H, I)
+    a, b = oracle.quantize_w4a16(synth.weights(32, 2 * Is, H))
+    c, d = oracle.quantize_w4a16(synth.weights(33, H, Is))
+    shared = (a, b, c, d)
+    base, _ = oracle.moe_ref(x, ids, rw, qgu, sgu, qdn, sdn, False, 1e-5)
+    # no shared expert: the routed layer
+    y0, _ = oracle.moe_block_ref(x, ids, rw, qgu, sgu, qdn, sdn, None, False, 1e-5)
+    np.testing.assert_array_equal(y0, base)
+    # a shared expert with all-zero scales adds nothing
+    y1, _ = oracle.moe_block_ref(x, ids, rw, qgu, sgu, qdn, sdn,
+                                 (a, np.zeros_like(b), c, np.zeros_like(d)), False, 1e-5)
+    np.testing.assert_allclose(y1, base, rtol=0, atol=1e-15)
+    # routing weights all zero: the shared expert alone, i.e. two GEMMs and SwiGLU
+    y2, tol2 = oracle.moe_block_ref(x, ids, np.zeros_like(rw), qgu, sgu, qdn, sdn, shared,
+                                    False, 1e-5)
+    gu, _ = oracle.gemm_ref(x, a, b)
+    h = oracle.silu(gu[:, :Is]) * gu[:, Is:]
+    yd = h @ oracle.dequantize(c, d).astype(np.float64).T   # h kept in fp64, as in fp32 mode
+    np.testing.assert_allclose(y2, yd, rtol=1e-12, atol=1e-14)
+    assert np.all(tol2 > 0)
+    # linearity in the routed part: block = routed layer + shared alone
+    y3, _ = oracle.moe_block_ref(x, ids, rw, qgu, sgu, qdn, sdn, shared, False, 1e-5)
+    np.testing.assert_allclose(y3, base + y2, rtol=1e-12, atol=1e-12)
