@@ -13,6 +13,8 @@ Other workloads are selectable with --config for the design notes:
   3 grouped MoE layer: 128 tokens, 384 experts, top-8, bf16  (TB/s of
     active-expert bytes)
   4 prefill GEMM 2048x7168 -> 18432 bf16     (TFLOP/s)
+  5 whole MoE block: config 3 plus the router and one shared expert
+    (width 2048), bf16                       (TB/s of active bytes)
 
 Timing: W warm-up steps, then exactly K steps captured in one CUDA graph
 and replayed once between barrier + synchronize, timed with CUDA events on
@@ -367,6 +369,78 @@ class MoeWorkload(Workload):
                                           f"({len(experts)} experts), scaled by token-slots")
 
 
+class MoeBlockWorkload(MoeWorkload):
+    """Whole MoE block: router (fp32 weights, sigmoid gate, top-8 of 384 with
+    a selection bias, scale 2.827), the routed layer of MoeWorkload and one
+    shared expert of width 2048; 128 tokens, hidden 7168, bf16."""
+
+    def __init__(self, w4, torch, dev, seed=0, T=128, H=7168, I=2048, E=384, topk=8, Is=2048):
+        import synth
+        super().__init__(w4, torch, dev, seed, T, H, I, E, topk)
+        self.name = (f"MoE block T={T} H={H} I={I} E={E} top-{topk} + shared expert "
+                     f"Is={Is}, router fp32, bf16")
+        self.Is = Is
+        self.scale = 2.827
+        self.wr = synth.weights_device(seed + 1, E, H, dev)
+        bias = synth.activations(seed + 1, 1, E)[0] * np.float32(0.05)
+        self.bias_np = bias
+        self.bias = torch.from_numpy(bias).to(dev)
+        self.shared = (w4.w4a16_quantize(synth.weights_device(seed, 2 * Is, H, dev, sub=2 * E)) +
+                       w4.w4a16_quantize(synth.weights_device(seed, H, Is, dev, sub=2 * E + 1)))
+        self.ws = torch.empty(w4.w4a16_moe_block_workspace_size(T, topk, E, H, I, Is),
+                              dtype=torch.uint8, device=dev)
+        # the device routing of this input fixes the active experts
+        _, ids, rw = w4.w4a16_moe_route(self.x, self.wr, topk, bias=self.bias,
+                                        route_scale=self.scale)
+        self.ids_np, self.rw_np = ids.cpu().numpy(), rw.cpu().numpy()
+        active = len(set(int(e) for e in self.ids_np.reshape(-1)))
+        self.active = active
+        per_expert = (2 * I * H // 2 + 2 * I * (H // 32) * 4) + (H * I // 2 + H * (I // 32) * 4)
+        shared_bytes = (2 * Is * H // 2 + 2 * Is * (H // 32) * 4) + (H * Is // 2 + H * (Is // 32) * 4)
+        self.bytes = (active * per_expert + shared_bytes + E * H * 4 + T * H * 2 + T * H * 4)
+        self.flops = 2.0 * T * (topk * (2 * I * H + H * I) + (2 * Is * H + H * Is) + E * H)
+        self.h2d = self.x_host.numel() * 2
+        self.d2h = T * H * 4
+        self.kernels_per_step = (2 + w4.w4a16_gemm_launches(T, 2 * Is, H, "bf16") + 1 +
+                                 w4.w4a16_gemm_launches(T, H, Is, "bf16") + 4)
+
+    def step(self, i, stream):
+        self.w4.w4a16_moe_block(self.x, self.wr, self.topk, self.qgu, self.sgu, self.qdn, self.sdn,
+                                shared=self.shared, bias=self.bias, route_scale=self.scale,
+                                workspace=self.ws, y=self.y, stream=stream)
+
+    def e2e_step(self, i, stream):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.step(i, stream)
+        self.y_host.copy_(self.y, non_blocking=True)
+        stream.synchronize()
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        tokens = [0, 1]
+        experts = {}
+        for t in tokens:
+            for e in self.ids_np[t]:
+                e = int(e)
+                if e not in experts:
+                    experts[e] = (self.qgu[e].cpu().numpy(), self.sgu[e].cpu().numpy(),
+                                  self.qdn[e].cpu().numpy(), self.sdn[e].cpu().numpy())
+        shared = tuple(v.cpu().numpy() for v in self.shared)
+        x = self.x_host.float().numpy()
+        wr = self.wr.cpu().numpy()
+        t1 = time.perf_counter()
+        oracle.moe_route_ref(x[tokens], wr, self.bias_np, self.topk, self.scale)
+        oracle.moe_block_ref(x, self.ids_np, self.rw_np, {e: v[0] for e, v in experts.items()},
+                             {e: v[1] for e, v in experts.items()},
+                             {e: v[2] for e, v in experts.items()},
+                             {e: v[3] for e, v in experts.items()}, shared, True, eps=4e-3,
+                             tokens=tokens)
+        el = time.perf_counter() - t1
+        full = el / len(tokens) * self.T
+        return self.bytes / full / 1e12, (f"oracle router + moe_block_ref on {len(tokens)} tokens "
+                                          f"({len(experts)} experts + shared), scaled by tokens")
+
+
 def make_workload(cfg, dtype, w4, torch, dev, overlap=True):
     if cfg == 0:
         return GemmWorkload(w4, torch, dev, 1, 512, 256, "f32", 0, "tiny GEMM M=1 K=256 N=512 fp32",
@@ -382,6 +456,8 @@ def make_workload(cfg, dtype, w4, torch, dev, overlap=True):
     if cfg == 4:
         return GemmWorkload(w4, torch, dev, 2048, 18432, 7168, "bf16", 0,
                             "prefill GEMM M=2048 K=7168 N=18432 bf16")
+    if cfg == 5:
+        return MoeBlockWorkload(w4, torch, dev)
     raise ValueError(cfg)
 
 
@@ -554,7 +630,8 @@ def run_ours(args):
                           if getattr(wl, "ncopies", 1) > 1 else "working set larger than L2"),
                    "timing": "one CUDA graph of K steps" if graph is not None else "eager launches",
                    "overlap": bool(getattr(wl, "overlap", False)),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"active_experts": wl.active} if hasattr(wl, "active") else {})},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
                 "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps},

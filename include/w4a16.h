@@ -224,6 +224,67 @@ w4a16_status w4a16_moe_gemm_noalloc(const void *x, w4a16_act_dtype xdt,
                                     int E, int H, int I, int group,
                                     float *y, w4a16_stream_t stream);
 
+/*
+ * w4a16_moe_route - the MoE router ("The Quiet Commit: ... Major Engineering
+ * Milestone", section "The Context: A Native DDTree Engine Takes Shape", and
+ * "The Quiet Commit: How a Single Plan Update Closed Phase 3 ...", section
+ * "The Context: Phase 3 of a Custom Inference Stack": DeepSeekV3/Kimi-style
+ * MoE routing; the pages give no formula, so the published DeepSeek-V3 gate
+ * is used):
+ *   logits[t][e] = x[t] . router_w[e]                  (fp32 accumulation)
+ *   s = sigmoid(logits); expert_ids[t] = the topk experts with the largest
+ *   s + router_bias, in decreasing order, equal values to the lower id;
+ *   route_w[t][j] = route_scale * s[t][ids[t][j]] / sum_j' s[t][ids[t][j']].
+ *   x [T][H] fp32 or bf16 (xdt), 16-byte aligned; H a multiple of 32
+ *   router_w [E][H] fp32, 16-byte aligned; router_bias [E] fp32 or NULL
+ *   logits [T][E] fp32, expert_ids [T][topk] int32, route_w [T][topk] fp32:
+ *   outputs, caller-owned device memory (overwritten).
+ * Errors: INVALID_ARG (null pointer, bad size, topk > E, route_scale not
+ * finite), UNSUPPORTED (E > 1024 or topk > 32), ALIGNMENT, CUDA.
+ */
+w4a16_status w4a16_moe_route(const void *x, w4a16_act_dtype xdt, int T, int H,
+                             const float *router_w, const float *router_bias, int E, int topk,
+                             float route_scale, float *logits, int32_t *expert_ids,
+                             float *route_w, w4a16_stream_t stream);
+
+/* Bytes of workspace w4a16_moe_block needs (0 for invalid sizes); Is = 0
+ * when there is no shared expert. */
+size_t w4a16_moe_block_workspace_size(int T, int topk, int E, int H, int I, int Is);
+
+/*
+ * w4a16_moe_block - the whole MoE block on INT4 experts: router, routed
+ * experts and the shared expert (same pages and sections as
+ * w4a16_moe_route and w4a16_moe_gemm; "The INT4 Milestone": the shared
+ * expert runs through the INT4 path too):
+ *   route as w4a16_moe_route (ids and weights written to expert_ids and
+ *   route_w), then
+ *   y[t] = sum_j route_w[t][j] * expert_{ids[t][j]}(x[t]) + shared(x[t]),
+ *   expert(x) = (silu(g) * u) * W_hat_dn^T with [g; u] = x * W_hat_gu^T
+ *   (h = silu(g) * u stored as bf16 in bf16 mode), the shared expert added
+ *   after the routed slots.
+ *   Routed experts as w4a16_moe_gemm: qw_gu [E][2I][H/8], sc_gu
+ *   [E][2I][H/group], qw_dn [E][H][I/8], sc_dn [E][H][I/group].
+ *   Shared expert of width Is: qw_sgu [2Is][H/8], sc_sgu [2Is][H/group],
+ *   qw_sdn [H][Is/8], sc_sdn [H][Is/group]; Is = 0 (pointers may be NULL)
+ *   means no shared expert. Its two projections run as w4a16_gemm calls.
+ *   workspace: at least w4a16_moe_block_workspace_size() bytes, 16-byte
+ *   aligned, caller-owned; contents on entry are ignored.
+ *   expert_ids [T][topk] int32, route_w [T][topk] fp32, y [T][H] fp32:
+ *   outputs (overwritten); y 16-byte aligned.
+ * group is 32, 64 or 128; H, I and Is multiples of group, at most 16384.
+ * Errors: as w4a16_moe_route and w4a16_moe_gemm.
+ */
+w4a16_status w4a16_moe_block(const void *x, w4a16_act_dtype xdt, int T,
+                             const float *router_w, const float *router_bias, int E, int topk,
+                             float route_scale,
+                             const int32_t *qw_gu, const float *sc_gu,
+                             const int32_t *qw_dn, const float *sc_dn, int H, int I,
+                             const int32_t *qw_sgu, const float *sc_sgu,
+                             const int32_t *qw_sdn, const float *sc_sdn, int Is,
+                             int group, void *workspace, size_t ws_bytes,
+                             int32_t *expert_ids, float *route_w, float *y,
+                             w4a16_stream_t stream);
+
 /* Testing aid for failure detection: when `enable` is non-zero, the next
  * launch of the streaming kernel on any device skips issuing its weight
  * copies, so its waits for them run out (after about one second) and it

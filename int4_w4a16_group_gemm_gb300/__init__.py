@@ -13,6 +13,12 @@ Functions keep the C names:
     w4a16_moe_workspace_size(T, topk, E, H, I) -> int
     w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn,
                    workspace=None, y=None, group=32, stream=None) -> y
+    w4a16_moe_route(x, router_w, topk, bias=None, route_scale=1.0, stream=None)
+        -> (logits, expert_ids, route_w)
+    w4a16_moe_block_workspace_size(T, topk, E, H, I, Is=0) -> int
+    w4a16_moe_block(x, router_w, topk, qw_gu, sc_gu, qw_dn, sc_dn, shared=None,
+                    bias=None, route_scale=1.0, group=32, workspace=None, y=None,
+                    stream=None) -> (y, expert_ids, route_w)
     w4a16_status_string(code) -> str
     w4a16_last_device_status(stream=None) -> int
 """
@@ -52,6 +58,13 @@ SIGNATURES = {
                             _VP, _SZ, _VP, _VP]),
     "w4a16_moe_gemm_noalloc": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I,
                                     _I, _VP, _VP]),
+    "w4a16_moe_route": (_I, [_VP, _I, _I, _I, _VP, _VP, _I, _I, ctypes.c_float, _VP, _VP, _VP,
+                             _VP]),
+    "w4a16_moe_block_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "w4a16_moe_block": (_I, [_VP, _I, _I, _VP, _VP, _I, _I, ctypes.c_float,
+                             _VP, _VP, _VP, _VP, _I, _I,
+                             _VP, _VP, _VP, _VP, _I,
+                             _I, _VP, _SZ, _VP, _VP, _VP, _VP]),
     "w4a16_debug_fault_next_launch": (None, [_I]),
     "w4a16_status_string": (ctypes.c_char_p, [_I]),
     "w4a16_last_device_status": (_I, [_VP]),
@@ -253,3 +266,73 @@ def w4a16_debug_fault_next_launch(enable: bool = True) -> None:
 
 def w4a16_last_device_status(stream=None) -> int:
     return int(lib.w4a16_last_device_status(_stream_handle(stream)))
+
+
+def w4a16_moe_route(x, router_w, topk: int, bias=None, route_scale: float = 1.0, stream=None):
+    """MoE router -> (logits fp32 [T, E], expert_ids int32 [T, topk], route_w fp32 [T, topk])."""
+    import torch
+    xdt = _act_dtype(x)
+    _need(x, x.dtype, "x")
+    _need(router_w, torch.float32, "router_w")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    T, H = x.shape
+    E = router_w.shape[0]
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    ids = torch.empty((T, topk), dtype=torch.int32, device=x.device)
+    rw = torch.empty((T, topk), dtype=torch.float32, device=x.device)
+    code = lib.w4a16_moe_route(_ptr(x), xdt, T, H, _ptr(router_w),
+                               _ptr(bias) if bias is not None else None, E, topk,
+                               float(route_scale), _ptr(logits), _ptr(ids), _ptr(rw),
+                               _stream_handle(stream))
+    _check("w4a16_moe_route", code)
+    return logits, ids, rw
+
+
+def w4a16_moe_block_workspace_size(T: int, topk: int, E: int, H: int, I: int, Is: int = 0) -> int:
+    return int(lib.w4a16_moe_block_workspace_size(T, topk, E, H, I, Is))
+
+
+def w4a16_moe_block(x, router_w, topk: int, qw_gu, sc_gu, qw_dn, sc_dn, shared=None, bias=None,
+                    route_scale: float = 1.0, group: int = 32, workspace=None, y=None,
+                    stream=None):
+    """Whole MoE block: router, routed experts and the shared expert.
+
+    ``shared`` is (qw_sgu [2Is, H/8], sc_sgu, qw_sdn [H, Is/8], sc_sdn) or None.
+    Returns (y fp32 [T, H], expert_ids int32 [T, topk], route_w fp32 [T, topk])."""
+    import torch
+    xdt = _act_dtype(x)
+    _need(x, x.dtype, "x")
+    _need(router_w, torch.float32, "router_w")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    for t, n, d in ((qw_gu, "qw_gu", torch.int32), (sc_gu, "sc_gu", torch.float32),
+                    (qw_dn, "qw_dn", torch.int32), (sc_dn, "sc_dn", torch.float32)):
+        _need(t, d, n)
+    T, H = x.shape
+    E = qw_gu.shape[0]
+    I = qw_gu.shape[1] // 2
+    if shared is not None:
+        for t, n, d in zip(shared, ("qw_sgu", "sc_sgu", "qw_sdn", "sc_sdn"),
+                           (torch.int32, torch.float32, torch.int32, torch.float32)):
+            _need(t, d, n)
+        Is = shared[0].shape[0] // 2
+        sp = [_ptr(t) for t in shared]
+    else:
+        Is = 0
+        sp = [None] * 4
+    ws = w4a16_moe_block_workspace_size(T, topk, E, H, I, Is)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=x.device)
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    ids = torch.empty((T, topk), dtype=torch.int32, device=x.device)
+    rw = torch.empty((T, topk), dtype=torch.float32, device=x.device)
+    code = lib.w4a16_moe_block(_ptr(x), xdt, T, _ptr(router_w),
+                               _ptr(bias) if bias is not None else None, E, topk,
+                               float(route_scale), _ptr(qw_gu), _ptr(sc_gu), _ptr(qw_dn),
+                               _ptr(sc_dn), H, I, sp[0], sp[1], sp[2], sp[3], Is, group,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _ptr(ids), _ptr(rw), _ptr(y), _stream_handle(stream))
+    _check("w4a16_moe_block", code)
+    return y, ids, rw

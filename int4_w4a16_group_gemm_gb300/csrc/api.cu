@@ -197,8 +197,119 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *e
     return W4A16_ERR_ALIGNMENT;
   if (!device_ready()) return W4A16_ERR_CUDA;
   return from_cuda(launch_moe(x, xdt == W4A16_ACT_BF16, expert_ids, route_w, T, topk, qw_gu,
-                              sc_gu, qw_dn, sc_dn, E, H, I, group, workspace, y,
+                              sc_gu, qw_dn, sc_dn, E, H, I, group, workspace, nullptr, y,
                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static constexpr int kRouterMaxExperts = 1024;
+static constexpr int kRouterMaxTopk = 32;
+
+static w4a16_status check_router(const void *x, w4a16_act_dtype xdt, int T, int H,
+                                 const float *router_w, int E, int topk, float route_scale) {
+  if (!x || !router_w) return W4A16_ERR_INVALID_ARG;
+  if (T <= 0 || H <= 0 || H % 32 != 0 || E <= 0 || topk <= 0 || topk > E)
+    return W4A16_ERR_INVALID_ARG;
+  if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
+  if (!(route_scale == route_scale) || route_scale == INFINITY || route_scale == -INFINITY)
+    return W4A16_ERR_INVALID_ARG;
+  if (E > kRouterMaxExperts || topk > kRouterMaxTopk) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(router_w)) return W4A16_ERR_ALIGNMENT;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_route(const void *x, w4a16_act_dtype xdt, int T, int H,
+                             const float *router_w, const float *router_bias, int E, int topk,
+                             float route_scale, float *logits, int32_t *expert_ids,
+                             float *route_w, w4a16_stream_t stream) {
+  const w4a16_status st = check_router(x, xdt, T, H, router_w, E, topk, route_scale);
+  if (st != W4A16_OK) return st;
+  if (!logits || !expert_ids || !route_w) return W4A16_ERR_INVALID_ARG;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  return from_cuda(launch_router(x, xdt == W4A16_ACT_BF16, T, H, router_w, router_bias, E, topk,
+                                 route_scale, logits, expert_ids, route_w,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Block workspace: the grouped layer's workspace, then the router logits
+// [T][E], the shared expert's gate/up output [T][2 Is], its SwiGLU output
+// [T][Is] and its down output [T][H] (fp32 each, 256-byte aligned).
+struct BlockWs {
+  size_t off_logits, off_gu, off_h, off_o, total;
+};
+
+static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+static BlockWs block_ws(int T, int topk, int E, int H, int I, int Is) {
+  BlockWs b{};
+  const size_t t = static_cast<size_t>(T);
+  b.off_logits = align256(moe_workspace_bytes(T, topk, E, H, I));
+  b.off_gu = b.off_logits + align256(t * E * sizeof(float));
+  b.off_h = b.off_gu + align256(t * 2 * Is * sizeof(float));
+  b.off_o = b.off_h + align256(t * Is * sizeof(float));
+  b.total = b.off_o + (Is > 0 ? align256(t * H * sizeof(float)) : 0);
+  return b;
+}
+
+size_t w4a16_moe_block_workspace_size(int T, int topk, int E, int H, int I, int Is) {
+  if (T < 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0 || Is < 0) return 0;
+  return block_ws(T, topk, E, H, I, Is).total;
+}
+
+w4a16_status w4a16_moe_block(const void *x, w4a16_act_dtype xdt, int T, const float *router_w,
+                             const float *router_bias, int E, int topk, float route_scale,
+                             const int32_t *qw_gu, const float *sc_gu, const int32_t *qw_dn,
+                             const float *sc_dn, int H, int I, const int32_t *qw_sgu,
+                             const float *sc_sgu, const int32_t *qw_sdn, const float *sc_sdn,
+                             int Is, int group, void *workspace, size_t ws_bytes,
+                             int32_t *expert_ids, float *route_w, float *y,
+                             w4a16_stream_t stream) {
+  w4a16_status st = check_router(x, xdt, T, H, router_w, E, topk, route_scale);
+  if (st != W4A16_OK) return st;
+  if (!qw_gu || !sc_gu || !qw_dn || !sc_dn || !workspace || !expert_ids || !route_w || !y)
+    return W4A16_ERR_INVALID_ARG;
+  if (I <= 0 || I % 32 != 0 || Is < 0 || Is % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (Is > 0 && (!qw_sgu || !sc_sgu || !qw_sdn || !sc_sdn)) return W4A16_ERR_INVALID_ARG;
+  if (!group_supported(group)) return W4A16_ERR_UNSUPPORTED;
+  if (H % group != 0 || I % group != 0 || Is % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (H > max_k_stream(1) || I > max_k_stream(1) || Is > max_k_stream(1))
+    return W4A16_ERR_UNSUPPORTED;
+  const BlockWs L = block_ws(T, topk, E, H, I, Is);
+  if (ws_bytes < L.total) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(qw_gu) || !aligned16(sc_gu) || !aligned16(qw_dn) || !aligned16(sc_dn) ||
+      !aligned16(workspace) || !aligned16(y))
+    return W4A16_ERR_ALIGNMENT;
+  if (Is > 0 && (!aligned16(qw_sgu) || !aligned16(sc_sgu) || !aligned16(qw_sdn) ||
+                 !aligned16(sc_sdn)))
+    return W4A16_ERR_ALIGNMENT;
+  if (!device_ready()) return W4A16_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const bool bf16 = xdt == W4A16_ACT_BF16;
+
+  // 1. router: logits, top-k ids and weights (into the caller's buffers)
+  st = from_cuda(launch_router(x, bf16, T, H, router_w, router_bias, E, topk, route_scale,
+                               reinterpret_cast<float *>(ws + L.off_logits), expert_ids, route_w,
+                               s));
+  if (st != W4A16_OK) return st;
+  // 2. shared expert: gate/up GEMM, SwiGLU, down GEMM (each GEMM on the
+  //    kernel its token count selects)
+  float *shared_o = nullptr;
+  if (Is > 0) {
+    float *gu = reinterpret_cast<float *>(ws + L.off_gu);
+    void *h = ws + L.off_h;
+    shared_o = reinterpret_cast<float *>(ws + L.off_o);
+    st = w4a16_gemm_ex(x, xdt, qw_sgu, sc_sgu, T, 2 * Is, H, group, gu, W4A16_ALGO_AUTO, 0u,
+                       stream);
+    if (st != W4A16_OK) return st;
+    st = from_cuda(launch_swiglu(gu, T, Is, bf16, h, s));
+    if (st != W4A16_OK) return st;
+    st = w4a16_gemm_ex(h, xdt, qw_sdn, sc_sdn, T, H, Is, group, shared_o, W4A16_ALGO_AUTO, 0u,
+                       stream);
+    if (st != W4A16_OK) return st;
+  }
+  // 3. routed experts: sort, gate/up + SwiGLU, down x weight, combine (+ shared)
+  return from_cuda(launch_moe(x, bf16, expert_ids, route_w, T, topk, qw_gu, sc_gu, qw_dn, sc_dn,
+                              E, H, I, group, ws, shared_o, y, s));
 }
 
 void w4a16_debug_fault_next_launch(int enable) { w4a16::g_fault_next.store(enable ? 1 : 0); }

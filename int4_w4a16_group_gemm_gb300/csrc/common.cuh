@@ -137,6 +137,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// SiLU in fp32: g * sigmoid(g).
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
 // Store element i of the output: fp32, or rounded to bf16 (to nearest,
 // ties to even) when `bf16` is set and y holds 16-bit elements.
 __device__ __forceinline__ void store_y(void *y, size_t i, float v, int bf16) {

@@ -65,9 +65,23 @@ cudaError_t launch_quantize(const float *w, int N, int K, int group, int32_t *qw
 cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *offsets,
                             int32_t *perm, cudaStream_t stream);
 size_t moe_workspace_bytes(int T, int topk, int E, int H, int I);
+// `shared_o` ([T][H] fp32, or nullptr) is added to every token's output
+// after its routed slots (the shared expert's output).
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
                        int T, int topk, const int32_t *qw_gu, const float *sc_gu,
                        const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
-                       int group, void *workspace, float *y, cudaStream_t stream);
+                       int group, void *workspace, const float *shared_o, float *y,
+                       cudaStream_t stream);
+
+// ------------------------------------------------------------ MoE block
+// Router: logits[T][E] = x W_r^T (fp32), then per token the topk experts by
+// sigmoid(logit) + bias (bias may be nullptr), ties to the lower id, and
+// weights scale * s_j / sum s (E <= 1024, topk <= 32).
+cudaError_t launch_router(const void *x, bool x_bf16, int T, int H, const float *router_w,
+                          const float *bias, int E, int topk, float scale, float *logits,
+                          int32_t *ids, float *route_w, cudaStream_t stream);
+// h[T][Is] = silu(gu[:, :Is]) * gu[:, Is:], bf16 or fp32.
+cudaError_t launch_swiglu(const float *gu, int T, int Is, bool h_bf16, void *h,
+                          cudaStream_t stream);
 
 }  // namespace w4a16

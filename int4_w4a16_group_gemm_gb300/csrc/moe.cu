@@ -18,7 +18,8 @@
 //               per sorted position (bf16 in bf16 mode);
 //  3. down:     the same over the down rows; o[p] = route_w[p] *
 //               (h @ W_dn^T), stored per pair;
-//  4. combine:  y[t] = o[t*topk + 0] + o[t*topk + 1] + ... (slot order).
+//  4. combine:  y[t] = o[t*topk + 0] + o[t*topk + 1] + ... (slot order),
+//               plus the shared expert's output of token t when given.
 // The work items of one expert are adjacent in the grid, so an expert's
 // weights come from HBM once and from L2 for its further token tiles.
 #include <algorithm>
@@ -149,8 +150,6 @@ struct MoeParams {
   int sc_bulk;
   int *status;
 };
-
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // Largest number of weight rows a CTA owns (bounds its table of per-warp
 // row sums).
@@ -365,7 +364,8 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 
 // ------------------------------------------------------------------ 4. combine
 __global__ void moe_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
-                                   int T, int topk, int H, int E, float *__restrict__ y) {
+                                   const float *__restrict__ shared, int T, int topk, int H,
+                                   int E, float *__restrict__ y) {
   const int H4 = H >> 2;
   const long long total = static_cast<long long>(T) * H4;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -383,6 +383,10 @@ __global__ void moe_combine_kernel(const float *__restrict__ o, const int32_t *_
       } else {
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
+    }
+    if (shared != nullptr) {  // the shared expert: one more slot, weight 1
+      const float4 v = reinterpret_cast<const float4 *>(shared + static_cast<size_t>(t) * H)[n4];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     reinterpret_cast<float4 *>(y + static_cast<size_t>(t) * H)[n4] = acc;
   }
@@ -481,7 +485,8 @@ size_t moe_workspace_bytes(int T, int topk, int E, int H, int I) {
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
                        int T, int topk, const int32_t *qw_gu, const float *sc_gu,
                        const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,
-                       int group, void *workspace, float *y, cudaStream_t stream) {
+                       int group, void *workspace, const float *shared_o, float *y,
+                       cudaStream_t stream) {
   const DeviceInfo &di = device_info();
   const WsLayout L = ws_layout(T, topk, E, H, I);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -528,7 +533,7 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
 
   const long long work = static_cast<long long>(T) * (H / 4);
   const int grid = static_cast<int>(std::min<long long>((work + 255) / 256, di.num_sms * 8ll));
-  moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, T, topk, H, E, y);
+  moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, shared_o, T, topk, H, E, y);
   return cudaGetLastError();
 }
 

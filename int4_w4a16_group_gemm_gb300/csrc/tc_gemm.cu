@@ -475,9 +475,16 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   const DeviceInfo &di = device_info();
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
-  // M <= 64: 128 x 64 tiles with K split over a cluster of up to 4 CTAs, so
-  // that every SM streams weights; otherwise 256 x 256 persistent tiles
-  const bool small = M <= 64;
+  // 128 x 64 tiles with K split over a cluster of up to 4 CTAs (so that
+  // every SM streams weights) for M <= 64, and for larger M while those
+  // tiles fit in one wave (measured at K = 7168: a one-wave split launch
+  // beats the persistent kernel up to M = 512); otherwise 256 x 256
+  // persistent tiles.
+  static const int env_variant = env_int("W4A16_TC_VARIANT");  // tuning override
+  const long long split_tiles = static_cast<long long>((M + 63) / 64) * ((N + 127) / 128);
+  bool small = M <= 64 || split_tiles <= di.num_sms;
+  if (env_variant == 1) small = true;
+  if (env_variant == 2) small = false;
   const int BM = small ? 64 : 256;
   const int ROWS = small ? 128 : 256;
   CUtensorMap tmap;

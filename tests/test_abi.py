@@ -101,3 +101,39 @@ def test_workspace_size_grows_with_tokens(w4):
     b = w4.w4a16_moe_workspace_size(256, 8, 384, 7168, 2048)
     assert 0 < a < b
     assert w4.w4a16_moe_workspace_size(-1, 8, 384, 7168, 2048) == 0
+
+
+def test_router_and_block_argument_checks_need_no_gpu(w4):
+    lib = w4.lib
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)
+    f = ctypes.c_float
+    route = lambda x, T, H, wr, E, k, scale: lib.w4a16_moe_route(  # noqa: E731
+        x, 0, T, H, wr, null, E, k, f(scale), fake, fake, fake, null)
+    assert route(null, 4, 64, fake, 8, 2, 1.0) == w4.W4A16_ERR_INVALID_ARG
+    assert route(fake, 4, 64, fake, 8, 9, 1.0) == w4.W4A16_ERR_INVALID_ARG      # topk > E
+    assert route(fake, 4, 48, fake, 8, 2, 1.0) == w4.W4A16_ERR_INVALID_ARG      # H % 32
+    assert route(fake, 4, 64, fake, 8, 2, float("nan")) == w4.W4A16_ERR_INVALID_ARG
+    assert route(fake, 4, 64, fake, 2000, 8, 1.0) == w4.W4A16_ERR_UNSUPPORTED   # E > 1024
+    assert route(fake, 4, 64, fake, 100, 40, 1.0) == w4.W4A16_ERR_UNSUPPORTED   # topk > 32
+    assert route(odd, 4, 64, fake, 8, 2, 1.0) == w4.W4A16_ERR_ALIGNMENT
+
+    # workspace: the grouped layer's, then logits and the shared expert's buffers
+    base = w4.w4a16_moe_workspace_size(128, 8, 384, 7168, 2048)
+    no_shared = w4.w4a16_moe_block_workspace_size(128, 8, 384, 7168, 2048, 0)
+    with_shared = w4.w4a16_moe_block_workspace_size(128, 8, 384, 7168, 2048, 2048)
+    assert base + 128 * 384 * 4 <= no_shared < with_shared
+    assert with_shared - no_shared >= 128 * (2 * 2048 + 2048 + 7168) * 4
+    assert w4.w4a16_moe_block_workspace_size(4, 2, 3, 64, 64, -1) == 0
+
+    def block(Is, sh, group=32, ws=None, H=64, I=64):
+        wsz = w4.w4a16_moe_block_workspace_size(4, 2, 3, H, I, max(Is, 0)) if ws is None else ws
+        return lib.w4a16_moe_block(fake, 1, 4, fake, null, 3, 2, f(1.0), fake, fake, fake, fake,
+                                   H, I, sh, sh, sh, sh, Is, group, fake, wsz, fake, fake, fake,
+                                   null)
+    assert block(64, null) == w4.W4A16_ERR_INVALID_ARG          # shared width, no weights
+    assert block(48, fake) == w4.W4A16_ERR_INVALID_ARG          # Is % 32
+    assert block(64, fake, group=128, H=128, I=128) == w4.W4A16_ERR_INVALID_ARG  # Is % group
+    assert block(64, fake, group=16) == w4.W4A16_ERR_UNSUPPORTED
+    assert block(64, fake, ws=100) == w4.W4A16_ERR_INVALID_ARG  # workspace too small

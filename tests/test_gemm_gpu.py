@@ -150,10 +150,15 @@ def test_gemm_on_side_stream(w4):
 @pytest.mark.parametrize("M,N,K", [
     (256, 256, 64), (1, 256, 96), (300, 300, 7168), (257, 513, 160), (64, 4096, 7168),
     (512, 1000, 2048), (31, 40, 4128),
+    # beyond 64 tokens with the split-K tiles in one wave
+    (128, 4096, 7168), (100, 1000, 4224), (200, 300, 1024), (512, 2048, 2048),
+    # the persistent 256 x 256 kernel (split tiles would exceed one wave), ragged
+    (600, 2100, 160), (1100, 1500, 2080),
 ])
 def test_tensor_core_path(w4, M, N, K):
-    """The tcgen05 kernel on one-tile, ragged (M, N not multiples of 256;
-    K % 64 == 32) and multi-tile shapes."""
+    """The tcgen05 kernels on one-tile, ragged (M, N not multiples of the
+    tile; K % 64 == 32) and multi-tile shapes: the split-K kernel up to one
+    wave of 64 x 128 tiles, the persistent kernel beyond."""
     run_case(w4, M, N, K, "bf16", seed=M + N + K, algo="tc")
 
 
