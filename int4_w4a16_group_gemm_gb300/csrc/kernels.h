@@ -49,6 +49,11 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
                            int N, int K, int group, void *y, bool y_bf16, bool overlap,
                            cudaStream_t stream);
 bool tc_gemm_supported(int M, int N, int K);
+// The small-M form of it (128 weight rows x 64 tokens per tile, K split over
+// a cluster of up to `kmax` CTAs, dequantised weights in tensor memory).
+cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
+                            int K, int group, void *y, bool y_bf16, bool overlap, int kmax,
+                            cudaStream_t stream);
 // fp32 activations on the tensor cores, exact to fp32 accumulation: each
 // activation is split into three bf16 pieces and the group scales are
 // applied in fp32 outside the MMA (M <= 64).

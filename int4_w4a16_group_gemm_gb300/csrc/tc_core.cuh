@@ -115,6 +115,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 8 packed nibbles (columns 0..7 of the word) * scale -> 8 bf16 in a uint4.
+// (nibble - 8) is formed exactly as an fp32 (see nibble_pair), multiplied by
+// the fp32 scale (one rounding, the format's own product), then rounded
+// once more to bf16.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, const NibbleConsts &k) {
+  const uint32_t w8 = w >> 8;
+  const uint64_t p[4] = {nibble_pair<0>(w, w8, k), nibble_pair<1>(w, w8, k),
+                         nibble_pair<2>(w, w8, k), nibble_pair<3>(w, w8, k)};
+  float v[8];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float sc = s * nibble_prescale(c);  // exact: a power-of-two scaling
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p[c]));
+    v[c] = lo * sc;
+    v[4 + c] = hi * sc;
+  }
+  uint4 o;
+  o.x = pack_bf16x2(v[0], v[1]);
+  o.y = pack_bf16x2(v[2], v[3]);
+  o.z = pack_bf16x2(v[4], v[5]);
+  o.w = pack_bf16x2(v[6], v[7]);
+  return o;
+}
+
+// Store 32 consecutive TMEM columns of this warp's 32 lanes (one 32-bit
+// value per lane and column); the caller waits with tmem_store_wait().
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_store_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// MMA with the A operand in tensor memory (M = 128 lanes, K-major, two bf16
+// per 32-bit column) and B in shared memory.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t dtmem, uint32_t atmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtmem),
+      "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Load 16 bytes from the shared memory of cluster rank `rank` at the
+// address of `p` in this CTA (p 16-byte aligned).
+__device__ __forceinline__ float4 ld_cluster_f32x4(const float *p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ bool aborted(const int *flag) {
   return *reinterpret_cast<const volatile int *>(flag) != 0;
 }

@@ -50,25 +50,27 @@ using namespace tc;
 constexpr int TC_BK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int A_SUB_BYTES = 128 * TC_BK * 2;        // 16 KB
 
-// Tile shapes. BM is the token width (the MMA N); SUBS the number of
+// Tile shape. BM is the token width (the MMA N); SUBS the number of
 // 128-row weight sub-tiles per CTA (each an MMA M = 128 with its own TMEM
-// accumulator of BM columns). Large M: BM = 256, SUBS = 2, persistent.
-// M <= 64: BM = 64, SUBS = 1, K split over a cluster.
+// accumulator of BM columns): BM = 256, SUBS = 2. (Small M runs on the
+// split-K kernel of tc_split.cu.)
 template <int BM, int SUBS>
 struct TcCfg {
-  static constexpr int kDqWarps = SUBS == 2 ? 8 : 16;      // dequantiser warps
+  static constexpr int kDqWarps = 8;                        // dequantiser warps
   static constexpr int kThreads = 64 + 32 * kDqWarps;      // + TMA warp + MMA warp
   static constexpr int kRows = 128 * SUBS;                 // weight rows per tile
   static constexpr int kABytes = SUBS * A_SUB_BYTES;
   static constexpr int kBBytes = BM * TC_BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = SUBS == 2 ? 3 : 8;
-  // stages of packed weights each dequant thread keeps in flight: deep when
-  // every weight comes from HBM (split K), shallow when tiles share them in L2
-  static constexpr int kPrefetch = SUBS == 2 ? 1 : 6;
+  static constexpr int kBlocks = 3;   // 64-column blocks in the ring
+  // blocks per pipeline stage (one barrier handshake per stage); a stage of
+  // this tile already carries 16 MMAs of N = 256
+  static constexpr int kSubK = 1;
+  static constexpr int kStages = kBlocks / kSubK;
+  static constexpr int kPrefetch = 1;  // stages of packed weights in flight per thread
   static constexpr int kThreadsPerRow = 32 * kDqWarps / kRows;  // dequant threads per row
   static constexpr int kTmemCols = SUBS * BM < 32 ? 32 : SUBS * BM;  // a power of two
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static constexpr int kSmem = kBlocks * kStageBytes + 1024 + 256;
   // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
   // 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
   // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -88,46 +90,15 @@ struct TcParams {
   int *status;
 };
 
-// 8 packed nibbles (columns 0..7 of the word) * scale -> 8 bf16 in a uint4.
-// (nibble - 8) is formed exactly as an fp32 (see nibble_pair), multiplied by
-// the fp32 scale (one rounding, the format's own product), then rounded
-// once more to bf16.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, const NibbleConsts &k) {
-  const uint32_t w8 = w >> 8;
-  const uint64_t p[4] = {nibble_pair<0>(w, w8, k), nibble_pair<1>(w, w8, k),
-                         nibble_pair<2>(w, w8, k), nibble_pair<3>(w, w8, k)};
-  float v[8];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float sc = s * nibble_prescale(c);  // exact: a power-of-two scaling
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p[c]));
-    v[c] = lo * sc;
-    v[4 + c] = hi * sc;
-  }
-  uint4 o;
-  o.x = pack_bf16x2(v[0], v[1]);
-  o.y = pack_bf16x2(v[2], v[3]);
-  o.z = pack_bf16x2(v[4], v[5]);
-  o.w = pack_bf16x2(v[6], v[7]);
-  return o;
-}
-
-
-// SPLIT = false: persistent CTAs walk the (weight-tile, token-tile) grid,
-//   each tile over all of K.
-// SPLIT = true: one tile per cluster; the cluster's CTAs (ranks along grid
-//   y) take consecutive K ranges. Each rank keeps the sum for a slice of
-//   the tile's rows: every CTA parks its fp32 partial tile in shared memory,
-//   pushes each owner's row slice into that owner's shared memory with one
-//   bulk copy, and the owner adds the slices in rank order (deterministic,
-//   no workspace).
-template <int BM, int SUBS, bool SPLIT>
+// Persistent CTAs walk the (weight-tile, token-tile) grid, each tile over
+// all of K.
+template <int BM, int SUBS>
 __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
   using Cfg = TcCfg<BM, SUBS>;
   constexpr int NS = Cfg::kStages;
-  constexpr int SB = Cfg::kStageBytes;
+  constexpr int SK = Cfg::kSubK;       // 64-column blocks per stage
+  constexpr int SB = Cfg::kStageBytes;  // bytes of one block (A then B)
   constexpr int PD = Cfg::kPrefetch;
   constexpr int ROWS = Cfg::kRows;
   constexpr int TPR = Cfg::kThreadsPerRow;
@@ -138,28 +109,20 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * SB);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * SK * SB);
   uint64_t *empty = full + NS;
   uint64_t *acc_full = empty + NS;
   uint64_t *acc_empty = acc_full + 1;
   uint64_t *drain = acc_empty + 1;
-  uint64_t *recv_bar = drain + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   const int nk = (K + TC_BK - 1) / TC_BK;
-  const int rank = SPLIT ? static_cast<int>(blockIdx.y) : 0;
-  const int ks = SPLIT ? static_cast<int>(gridDim.y) : 1;
-  // K blocks of this CTA, and its tiles
-  const int kb0 = SPLIT ? static_cast<int>((static_cast<long long>(nk) * rank) / ks) : 0;
-  const int kb1 = SPLIT ? static_cast<int>((static_cast<long long>(nk) * (rank + 1)) / ks) : nk;
+  const int kb0 = 0, kb1 = nk;  // every tile covers all of K
   const int tile_first = blockIdx.x;
-  const int tile_step = SPLIT ? p.num_tiles : gridDim.x;
-  // rows of the tile whose sum rank k keeps
-  auto slice_lo = [&](int k) { return (ROWS * k) / ks; };
-  const int my_rows = slice_lo(rank + 1) - slice_lo(rank);
+  const int tile_step = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -169,11 +132,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, DQ_WARPS);
     mbar_init(drain, 1);
-    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // this rank receives ks slices of my_rows x BM floats
-    if (SPLIT) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(ks * my_rows * BM * 4));
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -204,13 +164,16 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
       int it = 0;
       for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag); tile += tile_step) {
         const int m0 = (tile % p.tiles_m) * BM;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; kb += SK, ++it) {
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+          const int nsub = min(SK, kb1 - kb);
           if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
           if (aborted(abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], Cfg::kBBytes);
-          tma_load_2d(smem + s * SB + Cfg::kABytes, &tmap_x, kb * TC_BK, m0, &full[s]);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * Cfg::kBBytes));
+          for (int j = 0; j < nsub; ++j)
+            tma_load_2d(smem + (s * SK + j) * SB + Cfg::kABytes, &tmap_x, (kb + j) * TC_BK, m0,
+                        &full[s]);
         }
       }
     }
@@ -227,19 +190,22 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         }
         tc_fence_after();
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; kb += SK, ++it) {
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+          const int nsub = min(SK, kb1 - kb);
           if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * SB);
-          const uint32_t b0 = a0 + Cfg::kABytes;
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t a0 = smem_u32(smem + (s * SK + j) * SB);
+            const uint32_t b0 = a0 + Cfg::kABytes;
 #pragma unroll
-          for (int sub = 0; sub < SUBS; ++sub)
+            for (int sub = 0; sub < SUBS; ++sub)
 #pragma unroll
-            for (int k = 0; k < TC_BK / 16; ++k)
-              tc_mma(tmem + sub * BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
-                     sw128_desc(b0 + k * 32), Cfg::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < TC_BK / 16; ++k)
+                tc_mma(tmem + sub * BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
+                       sw128_desc(b0 + k * 32), Cfg::kIdesc, (kb + j > kb0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(&empty[s]);
           issued_any = true;
         }
@@ -277,9 +243,9 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
       const float *srow = p.sc + static_cast<size_t>(n) * G;
 
       // register ring of PD prefetched stages (slots indexed at compile time);
-      // each stage of this thread: WPT words and their scale(s)
-      uint32_t ra[PD][WPT];
-      float rs[PD][PIECES];
+      // each stage of this thread: SK blocks of WPT words and their scale(s)
+      uint32_t ra[PD][SK][WPT];
+      float rs[PD][SK][PIECES];
       auto fetch = [&](int kb, uint32_t (&w)[WPT], float (&sc)[PIECES]) {
 #pragma unroll
         for (int i = 0; i < WPT; ++i) w[i] = 0u;
@@ -305,32 +271,46 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         }
       };
 #pragma unroll
-      for (int u = 0; u < PD; ++u) fetch(kb0 + u, ra[u], rs[u]);
+      for (int u = 0; u < PD; ++u)
+#pragma unroll
+        for (int j = 0; j < SK; ++j) fetch(kb0 + u * SK + j, ra[u][j], rs[u][j]);
       bool ok = true;
-      for (int kbase = kb0; kbase < kb1 && ok; kbase += PD) {
+      // one stage (SK blocks) per iteration: the SK blocks' words are
+      // independent, so their dequantisation interleaves
+      for (int kbase = kb0; kbase < kb1 && ok; kbase += PD * SK) {
 #pragma unroll
         for (int u = 0; u < PD; ++u) {
-          const int kb = kbase + u;
-          if (kb >= kb1) break;
+          const int kbs = kbase + u * SK;  // first block of the stage
+          if (kbs >= kb1) break;
+          const int nsub = min(SK, kb1 - kbs);
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           ++it;
-          uint32_t cw[WPT];
-          float cs[PIECES];
+          uint32_t cw[SK][WPT];
+          float cs[SK][PIECES];
 #pragma unroll
-          for (int i = 0; i < WPT; ++i) cw[i] = ra[u][i];
+          for (int j = 0; j < SK; ++j) {
 #pragma unroll
-          for (int h = 0; h < PIECES; ++h) cs[h] = rs[u][h];
-          fetch(kb + PD, ra[u], rs[u]);
+            for (int i = 0; i < WPT; ++i) cw[j][i] = ra[u][j][i];
+#pragma unroll
+            for (int h = 0; h < PIECES; ++h) cs[j][h] = rs[u][j][h];
+          }
+#pragma unroll
+          for (int j = 0; j < SK; ++j) fetch(kbs + PD * SK + j, ra[u][j], rs[u][j]);
           const bool got =
               __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
           if (!got) { fail(); ok = false; break; }
-          uint8_t *arow = smem + s * SB + row_off;
 #pragma unroll
-          for (int i = 0; i < WPT; ++i) {
-            const int chunk = part * WPT + i;
-            *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) =
-                dequant_word(cw[i], cs[i / PW], nk);
+          for (int j = 0; j < SK; ++j) {
+            if (j < nsub) {
+              uint8_t *arow = smem + (s * SK + j) * SB + row_off;
+#pragma unroll
+              for (int i = 0; i < WPT; ++i) {
+                const int chunk = part * WPT + i;
+                *reinterpret_cast<uint4 *>(arow + ((chunk ^ swz) << 4)) =
+                    dequant_word(cw[j][i], cs[j][i / PW], nk);
+              }
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -349,33 +329,19 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
         const int nl = esub * 128 + q * 32 + lane;  // row within the tile
         const int ne = n0 + nl;
         const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + esub * BM;
-        // split: partial tile to shared memory, row-major with the elements
-        // of each row rotated by the row index (column m of row r at
-        // (m + r) mod BM), so that the 32 lanes of a warp, 32 consecutive
-        // rows at one column, hit 32 different banks; the stages are idle
-        float *red = reinterpret_cast<float *>(smem);
 #pragma unroll 1
         for (int cc = 0; cc < BM / 32; ++cc) {
           uint32_t r[32];
           tmem_ld_32cols(tbase + cc * 32, r);
-          if (SPLIT) {
+          const int mb = m0 + cc * 32;
+          if (ne < p.N) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = cc * 32 + j;
-              red[nl * BM + ((m + nl) & (BM - 1))] = __uint_as_float(r[j]);
-            }
-          } else {
-            const int mb = m0 + cc * 32;
-            if (ne < p.N) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (mb + j < p.M)
-                  store_y(p.y, static_cast<size_t>(mb + j) * p.N + ne, __uint_as_float(r[j]),
-                          p.ybf16);
-            }
+            for (int j = 0; j < 32; ++j)
+              if (mb + j < p.M)
+                store_y(p.y, static_cast<size_t>(mb + j) * p.N + ne, __uint_as_float(r[j]),
+                        p.ybf16);
           }
         }
-        if (SPLIT) fence_proxy_async_smem();  // the bulk copies read `red`
       }
       tc_fence_before();
       __syncwarp();
@@ -383,41 +349,6 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     }
   }
   __syncthreads();
-  if (SPLIT) {
-    griddep_wait();  // every thread writes y below
-    // every CTA of the cluster has parked its partial tile
-    cluster_sync_all();
-    const int n0 = (tile_first / p.tiles_m) * ROWS;
-    const int m0 = (tile_first % p.tiles_m) * BM;
-    const float *red = reinterpret_cast<const float *>(smem);
-    const float *recv = red + ROWS * BM;  // [ks][my_rows][BM]
-    const bool ok_here = *reinterpret_cast<volatile int *>(abort_flag) == 0;
-    if (threadIdx.x == 0) {
-      // push owner k's rows of this partial tile into its receive area
-      for (int k = 0; k < ks; ++k) {
-        const int lo = slice_lo(k), rows_k = slice_lo(k + 1) - lo;
-        const uint32_t dst = cluster_map(smem_u32(recv + rank * rows_k * BM), k);
-        bulk_s2cluster(dst, red + lo * BM, static_cast<uint32_t>(rows_k * BM * 4),
-                       cluster_map(smem_u32(recv_bar), k));
-      }
-    }
-    const bool got = mbar_wait(recv_bar, 0);
-    if (!got) fail();
-    if (got && ok_here) {
-      const int lo = slice_lo(rank);
-      for (int e = threadIdx.x; e < my_rows * BM; e += blockDim.x) {
-        const int i = e % my_rows, m = e / my_rows;  // consecutive threads: consecutive rows
-        const int nl = lo + i;
-        if (n0 + nl >= p.N || m0 + m >= p.M) continue;
-        const int col = (m + nl) & (BM - 1);
-        float v = recv[i * BM + col];
-        for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * BM + col];
-        store_y(p.y, static_cast<size_t>(m0 + m) * p.N + n0 + nl, v, p.ybf16);
-      }
-    }
-    // no CTA leaves while its shared memory may still be copied from
-    cluster_sync_all();
-  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -434,11 +365,11 @@ bool tc_gemm_supported(int M, int N, int K) {
 
 namespace {
 
-template <int BM, int SUBS, bool SPLIT>
-cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, int ks,
-                      bool overlap, cudaStream_t stream) {
+template <int BM, int SUBS>
+cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, bool overlap,
+                      cudaStream_t stream) {
   using Cfg = TcCfg<BM, SUBS>;
-  auto kern = tc_gemm_kernel<BM, SUBS, SPLIT>;
+  auto kern = tc_gemm_kernel<BM, SUBS>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -446,19 +377,15 @@ cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, in
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_x, SPLIT ? ks : 1);
+  cfg.gridDim = dim3(grid_x);
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = SPLIT ? ks : 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tmap, p);
 }
 
@@ -473,20 +400,23 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
                            int K, int group, void *y, bool y_bf16, bool overlap,
                            cudaStream_t stream) {
   const DeviceInfo &di = device_info();
-  auto encode = encode_fn();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  // 128 x 64 tiles with K split over a cluster of up to 4 CTAs (so that
-  // every SM streams weights) for M <= 64, and for larger M while those
-  // tiles fit in one wave (measured at K = 7168: a one-wave split launch
-  // beats the persistent kernel up to M = 512); otherwise 256 x 256
-  // persistent tiles.
+  // 128 x 64 tiles with K split over a cluster (tc_split.cu) for M <= 64,
+  // and for larger M while those tiles fit in one wave (measured at
+  // K = 7168: a one-wave split launch beats the persistent kernel up to
+  // M = 512); otherwise 256 x 256 persistent tiles here.
   static const int env_variant = env_int("W4A16_TC_VARIANT");  // tuning override
   const long long split_tiles = static_cast<long long>((M + 63) / 64) * ((N + 127) / 128);
   bool small = M <= 64 || split_tiles <= di.num_sms;
   if (env_variant == 1) small = true;
   if (env_variant == 2) small = false;
-  const int BM = small ? 64 : 256;
-  const int ROWS = small ? 128 : 256;
+  if (small) {
+    static const int env_ks = env_int("W4A16_TC_KS");  // tuning override
+    const int kmax = env_ks > 0 ? std::min(env_ks, 8) : 4;
+    return launch_tc_split(x, qw, sc, M, N, K, group, y, y_bf16, overlap, kmax, stream);
+  }
+  auto encode = encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  constexpr int BM = 256, ROWS = 256;
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
@@ -506,19 +436,10 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   p.N = N;
   p.K = K;
   p.tiles_m = (M + BM - 1) / BM;
-  const int tiles_n = (N + ROWS - 1) / ROWS;
-  p.num_tiles = p.tiles_m * tiles_n;
+  p.num_tiles = p.tiles_m * ((N + ROWS - 1) / ROWS);
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
-  if (small) {
-    static const int env_ks = env_int("W4A16_TC_KS");  // tuning override
-    const int kmax = env_ks > 0 ? std::min(env_ks, 8) : 4;
-    const int nk = (K + TC_BK - 1) / TC_BK;
-    const int ks = std::max(1, std::min(std::min(kmax, nk), di.num_sms / std::max(1, p.num_tiles)));
-    return launch_tc<64, 1, true>(tmap, p, p.num_tiles, ks, overlap, stream);
-  }
-  return launch_tc<256, 2, false>(tmap, p, std::min(p.num_tiles, di.num_sms), 1, overlap,
-                                   stream);
+  return launch_tc<BM, 2>(tmap, p, std::min(p.num_tiles, di.num_sms), overlap, stream);
 }
 
 }  // namespace w4a16

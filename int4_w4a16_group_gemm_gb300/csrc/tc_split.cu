@@ -1,0 +1,389 @@
+// Small-M W4A16 GEMM on the tcgen05 tensor cores (bf16 activations), with
+// the dequantised weights kept in tensor memory and K split over a cluster.
+//
+//   y[m][n] = sum_k x[m][k] * W_hat[n][k],  W_hat = (nibble - 8) * scale
+//
+// As in the large-M kernel the product is computed transposed, D[n][m]: the
+// 128 weight rows of a tile are the MMA's M, 64 tokens its N. At this size
+// the dequantised A tile is the bandwidth problem: written to shared memory
+// by the CUDA cores and read back by every MMA, it costs 4 bytes of
+// shared-memory traffic per weight, which is what bounds a shared-memory-A
+// kernel here. So the dequantisers store A straight into tensor memory
+// (tcgen05.st) and the MMAs read it from there (the A-in-TMEM form of
+// tcgen05.mma); shared memory only carries the activations (TMA).
+//
+// Tile: 128 weight rows x 64 tokens, K split over a cluster of ks CTAs
+// (grid y = rank). Pipeline stage = 4 blocks of 64 K columns, 3 stages:
+//   warp 0       TMA: one 64 x 64 bf16 activation box (128-byte swizzle)
+//                per block into the stage's B slot;
+//   warp 1       TMEM owner and MMA issuer: per stage, 4 x 4 MMAs
+//                (M=128, N=64, K=16) with A from TMEM, one commit;
+//   warps 2-17   dequantisers: warp w handles block (w - 2) / 4 of every
+//                stage for TMEM lane quadrant w % 4; thread = weight row,
+//                8 packed words (64 columns) per block, dequantised to
+//                bf16 pairs and stored as 32 TMEM columns.
+// TMEM: columns 0-63 the fp32 accumulator, 64 + 32 * (stage * 4 + block)
+// the A blocks (448 of 512 columns).
+// Epilogue: each rank parks its fp32 partial tile in shared memory; after a
+// cluster barrier the owner of a row slice reads the slice from every rank
+// (distributed shared memory) and adds the partials in rank order, so the
+// result is deterministic and needs no workspace.
+// Every wait is bounded; a timeout is recorded in the status word and the
+// CTA unwinds (TMEM is always freed).
+//
+// Format: "The Quiet Commit: How a Single Documentation Edit Marks the
+// Completion of a Major Engineering Milestone", section "The INT4 Milestone".
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_core.cuh"
+
+namespace w4a16 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int SP_BM = 64;          // tokens per tile (MMA N)
+constexpr int SP_ROWS = 128;       // weight rows per tile (MMA M)
+constexpr int SP_BK = 64;          // K columns per block
+constexpr int SP_SK = 4;           // blocks per stage
+constexpr int SP_NS = 3;           // stages
+constexpr int SP_DQ_WARPS = 16;    // 4 blocks x 4 lane quadrants
+constexpr int SP_THREADS = 64 + 32 * SP_DQ_WARPS;
+constexpr int SP_B_BYTES = SP_BM * SP_BK * 2;               // 8 KB per block
+constexpr int SP_ACC_COLS = SP_BM;                          // fp32 accumulator
+constexpr int SP_A_COL0 = SP_ACC_COLS;                      // first A block column
+constexpr int SP_TMEM_COLS = 512;
+constexpr int SP_RING_BYTES = SP_NS * SP_SK * SP_B_BYTES;   // 96 KB
+constexpr int SP_SMEM = SP_RING_BYTES + 1024 + 256;
+constexpr int SP_RED_LD = SP_BM + 4;  // row stride of the parked partial tile (floats)
+constexpr int SP_MAX_KS = 8;          // largest cluster (K split)
+static_assert(SP_A_COL0 + SP_NS * SP_SK * 32 <= SP_TMEM_COLS, "TMEM budget");
+static_assert(SP_ROWS * (SP_BM + 4) * 4 <= SP_RING_BYTES, "parked partial tile");
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
+// N = 64, M = 128.
+constexpr uint32_t SP_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                              (static_cast<uint32_t>(SP_BM >> 3) << 17) |
+                              (static_cast<uint32_t>(128 >> 4) << 24);
+
+struct SpParams {
+  const int32_t *qw;
+  const float *sc;
+  void *y;  // fp32, or bf16 when ybf16
+  int ybf16;
+  int M, N, K;
+  int tiles_m, num_tiles;
+  int gs;  // log2 of the group size
+  int *status;
+};
+
+__global__ void __launch_bounds__(SP_THREADS, 1)
+    tc_split_kernel(const __grid_constant__ CUtensorMap tmap_x, const SpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SP_RING_BYTES);
+  uint64_t *empty = full + SP_NS;
+  uint64_t *acc_full = empty + SP_NS;
+  uint64_t *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K;
+  const int nk = (K + SP_BK - 1) / SP_BK;
+  const int rank = static_cast<int>(blockIdx.y);
+  const int ks = static_cast<int>(gridDim.y);
+  const int kb0 = static_cast<int>((static_cast<long long>(nk) * rank) / ks);
+  const int kb1 = static_cast<int>((static_cast<long long>(nk) * (rank + 1)) / ks);
+  const int tile = blockIdx.x;
+  const int n0 = (tile / p.tiles_m) * SP_ROWS;
+  const int m0 = (tile % p.tiles_m) * SP_BM;
+  auto slice_lo = [&](int k) { return (SP_ROWS * k) / ks; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SP_NS; ++s) {
+      mbar_init(&full[s], 1 + SP_DQ_WARPS);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(SP_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Programmatic launch: the weights are read before griddep_wait (never
+  // written by the previous kernel, by the overlap contract), x and y after.
+  griddep_launch_dependents();
+
+  auto fail = [&]() {
+    record_status(p.status, W4A16_ERR_TIMEOUT);
+    *reinterpret_cast<volatile int *>(abort_flag) = 1;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      griddep_wait();
+      int it = 0;
+      for (int kb = kb0; kb < kb1 && !aborted(abort_flag); kb += SP_SK, ++it) {
+        const int s = it % SP_NS;
+        const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
+        const int nsub = min(SP_SK, kb1 - kb);
+        if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
+        if (aborted(abort_flag)) break;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * SP_B_BYTES));
+        for (int j = 0; j < nsub; ++j)
+          tma_load_2d(smem + (s * SP_SK + j) * SP_B_BYTES, &tmap_x, (kb + j) * SP_BK, m0,
+                      &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0;
+      bool issued_any = false, ok = true;
+      for (int kb = kb0; kb < kb1; kb += SP_SK, ++it) {
+        const int s = it % SP_NS;
+        const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
+        const int nsub = min(SP_SK, kb1 - kb);
+        if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
+        tc_fence_after();
+        for (int j = 0; j < nsub; ++j) {
+          const uint32_t a0 = tmem + SP_A_COL0 + (s * SP_SK + j) * 32;
+          const uint32_t b0 = smem_u32(smem + (s * SP_SK + j) * SP_B_BYTES);
+#pragma unroll
+          for (int k = 0; k < SP_BK / 16; ++k)
+            tc_mma_tmem_a(tmem, a0 + k * 8, sw128_desc(b0 + k * 32), SP_IDESC,
+                          (kb + j > kb0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+        issued_any = true;
+      }
+      if (ok) tc_commit(acc_full);
+      // all MMAs this thread issued are complete before TMEM is released
+      if (issued_any) {
+        tc_commit(drain);
+        mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- dequantisers
+    const NibbleConsts nk_ = make_nibble_consts();
+    const int dw = warp - 2;
+    const int j = dw >> 2;                 // block of the stage this warp fills
+    const int q = warp & 3;                // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;         // weight row within the tile = TMEM lane
+    const int n = n0 + row;
+    const bool nvalid = n < p.N;
+    const int Kw = K >> 3;
+    const int G = K >> p.gs;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.qw) +
+                           static_cast<size_t>(nvalid ? n : 0) * Kw;
+    const float *srow = p.sc + static_cast<size_t>(nvalid ? n : 0) * G;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+
+    // the 8 packed words (2 x 16 B) and 2 scales of this row in block kb
+    auto fetch = [&](int kb, uint4 (&w)[2], float (&sc)[2]) {
+      w[0] = w[1] = make_uint4(0, 0, 0, 0);
+      sc[0] = sc[1] = 0.f;
+      if (!nvalid || kb >= kb1) return;
+      const int w0 = kb * 8;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (w0 + 4 * h < Kw) {
+          w[h] = __ldg(reinterpret_cast<const uint4 *>(qrow + w0 + 4 * h));
+          sc[h] = __ldg(srow + (((w0 + 4 * h) * 8) >> p.gs));  // 32 columns, one group
+        }
+      }
+    };
+    // two stages of this warp's block in flight
+    uint4 rw[2][2];
+    float rsc[2][2];
+    fetch(kb0 + j, rw[0], rsc[0]);
+    fetch(kb0 + SP_SK + j, rw[1], rsc[1]);
+    int it = 0;
+    bool ok = true;
+    for (int kbase = kb0; kbase < kb1 && ok; kbase += 2 * SP_SK) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int kbs = kbase + u * SP_SK;  // first block of the stage
+        if (kbs >= kb1) break;
+        const int s = it % SP_NS;
+        const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
+        ++it;
+        const uint4 cw[2] = {rw[u][0], rw[u][1]};
+        const float cs[2] = {rsc[u][0], rsc[u][1]};
+        fetch(kbs + 2 * SP_SK + j, rw[u], rsc[u]);
+        const bool got =
+            __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
+        if (!got) { fail(); ok = false; break; }
+        tc_fence_after();
+        if (kbs + j < kb1) {
+          uint32_t a[32];
+          const uint32_t wv[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w,
+                                  cw[1].x, cw[1].y, cw[1].z, cw[1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 d = dequant_word(wv[i], cs[i >> 2], nk_);
+            a[4 * i] = d.x; a[4 * i + 1] = d.y; a[4 * i + 2] = d.z; a[4 * i + 3] = d.w;
+          }
+          tmem_st_32cols(lane_base + SP_A_COL0 + (s * SP_SK + j) * 32, a);
+          tmem_store_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+    }
+    if (ok) {
+      // partial tile -> shared memory (the ring is idle once acc_full
+      // completes): row r at red[r * SP_RED_LD], 16-byte stores; the padded
+      // row stride puts 8 consecutive rows' chunks in 8 different bank groups
+      if (j == 0) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full, 0))) {
+          fail();
+        } else {
+          tc_fence_after();
+          float *red = reinterpret_cast<float *>(smem) + row * SP_RED_LD;
+#pragma unroll 1
+          for (int cc = 0; cc < SP_BM / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld_32cols(lane_base + cc * 32, r);
+#pragma unroll
+            for (int t = 0; t < 32; t += 4)
+              *reinterpret_cast<uint4 *>(red + cc * 32 + t) =
+                  make_uint4(r[t], r[t + 1], r[t + 2], r[t + 3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  // every CTA of the cluster has parked its partial tile (or failed)
+  cluster_sync_all();
+  griddep_wait();  // every thread may write y below
+  {
+    const bool ok_all = *reinterpret_cast<volatile int *>(abort_flag) == 0;
+    const int lo = slice_lo(rank), my_rows = slice_lo(rank + 1) - lo;
+    const float *red = reinterpret_cast<const float *>(smem);
+    if (ok_all) {
+      // owner of rows lo .. lo + my_rows - 1: read 4 columns of a row from
+      // every rank (16-byte distributed shared-memory loads, all issued
+      // before the sums) and add them in rank order; consecutive threads
+      // take consecutive rows, so the y stores coalesce
+      for (int e = threadIdx.x; e < my_rows * (SP_BM / 4); e += blockDim.x) {
+        const int i = e % my_rows, c4 = e / my_rows;
+        const int nl = lo + i;
+        const float *src = red + nl * SP_RED_LD + 4 * c4;
+        float4 part[SP_MAX_KS];
+#pragma unroll
+        for (int k = 0; k < SP_MAX_KS; ++k)
+          if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
+        float4 v = part[0];
+#pragma unroll
+        for (int k = 1; k < SP_MAX_KS; ++k)
+          if (k < ks) {
+            v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
+          }
+        if (n0 + nl >= p.N) continue;
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int m = 4 * c4 + t;
+          if (m0 + m < p.M) store_y(p.y, static_cast<size_t>(m0 + m) * p.N + n0 + nl, vv[t], p.ybf16);
+        }
+      }
+    }
+  }
+  // no CTA leaves while its shared memory may still be read
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(SP_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *sc, int M, int N,
+                            int K, int group, void *y, bool y_bf16, bool overlap, int kmax,
+                            cudaStream_t stream) {
+  const DeviceInfo &di = device_info();
+  auto encode = encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {SP_BK, SP_BM};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  SpParams p{};
+  p.qw = qw;
+  p.sc = sc;
+  p.y = y;
+  p.ybf16 = y_bf16 ? 1 : 0;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + SP_BM - 1) / SP_BM;
+  p.num_tiles = p.tiles_m * ((N + SP_ROWS - 1) / SP_ROWS);
+  p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
+  p.status = di.status;
+  // split K over a cluster of up to kmax CTAs (a power of two) so that the
+  // clusters cover the SMs once
+  const int nk = (K + SP_BK - 1) / SP_BK;
+  int ks = 1;
+  while (2 * ks <= std::min(std::min(std::min(kmax, SP_MAX_KS), nk),
+                            di.num_sms / std::max(1, p.num_tiles)))
+    ks *= 2;
+
+  auto kern = tc_split_kernel;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_tiles, ks);
+  cfg.blockDim = dim3(SP_THREADS);
+  cfg.dynamicSmemBytes = SP_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = ks;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+}
+
+}  // namespace w4a16
