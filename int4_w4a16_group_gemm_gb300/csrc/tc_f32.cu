@@ -76,6 +76,9 @@ constexpr int FX_NB = 3 * FX_BM;    // MMA N: the three activation pieces side b
 constexpr int FX_ACC = 2;           // group accumulators in TMEM (FX_NB columns each)
 constexpr int FX_TMEM_COLS = 512;   // FX_ACC * FX_NB rounded up to a power of two
 constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + 1024 + 256;
+constexpr int FX_RED_LD = FX_BM + 4;  // row stride of the parked partial tile (floats)
+constexpr int FX_MAX_KS = 4;          // largest cluster (K split)
+static_assert(FX_ROWS * FX_RED_LD * 4 <= FX_NS * FX_STAGE, "parked partial tile");
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
 // N = 192 (the three 64-row piece tiles are one K-major B tile), M = 128.
 constexpr uint32_t FX_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -149,8 +152,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   uint64_t *acc_full = empty + NS;                                 // [FX_ACC] group sum ready
   uint64_t *acc_empty = acc_full + FX_ACC;                         // [FX_ACC] group sum read
   uint64_t *drain = acc_empty + FX_ACC;
-  uint64_t *recv_bar = drain + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,10 +185,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
       mbar_init(&acc_empty[b], FX_RB_WARPS);
     }
     mbar_init(drain, 1);
-    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(ks * my_rows * FX_BM * 4));
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -388,14 +388,13 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     }
     if (ok) {
       // partial tile to shared memory (the pipeline stages are idle once
-      // every group has been read), row-major with the elements of row r
-      // rotated by r (column m at (m + r) mod 64): conflict-free for 32
-      // consecutive rows at one column
-      float *red = reinterpret_cast<float *>(smem);
+      // every group has been read): row r at red[r * FX_RED_LD], 16-byte
+      // stores; the padded stride puts 8 consecutive rows' chunks in 8
+      // different bank groups
+      float *red = reinterpret_cast<float *>(smem) + r * FX_RED_LD;
 #pragma unroll
-      for (int m = 0; m < FX_BM; ++m)
-        red[r * FX_BM + ((m + r) & (FX_BM - 1))] = acc[m];
-      fence_proxy_async_smem();  // the bulk copies read `red`
+      for (int m = 0; m < FX_BM; m += 4)
+        *reinterpret_cast<float4 *>(red + m) = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
     }
   }
 
@@ -405,31 +404,37 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   cluster_sync_all();  // every CTA of the cluster has parked its partial tile
   {
     const float *red = reinterpret_cast<const float *>(smem);
-    const float *recv = red + FX_ROWS * FX_BM;  // [ks][my_rows][BM]
     const bool ok_here = *reinterpret_cast<volatile int *>(abort_flag) == 0;
-    if (threadIdx.x == 0) {
-      for (int k = 0; k < ks; ++k) {
-        const int lo = slice_lo(k), rows_k = slice_lo(k + 1) - lo;
-        const uint32_t dst = cluster_map(smem_u32(recv + rank * rows_k * FX_BM), k);
-        bulk_s2cluster(dst, red + lo * FX_BM, static_cast<uint32_t>(rows_k * FX_BM * 4),
-                       cluster_map(smem_u32(recv_bar), k));
-      }
-    }
-    const bool got = mbar_wait(recv_bar, 0);
-    if (!got) fail();
-    if (got && ok_here) {
+    if (ok_here) {
+      // owner of rows lo .. lo + my_rows - 1: read 4 columns of a row from
+      // every rank (16-byte distributed shared-memory loads, all issued
+      // before the sums) and add them in rank order; consecutive threads
+      // take consecutive rows, so the y stores coalesce
       const int lo = slice_lo(rank);
-      for (int e = threadIdx.x; e < my_rows * FX_BM; e += blockDim.x) {
-        const int i = e % my_rows, m = e / my_rows;
+      for (int e = threadIdx.x; e < my_rows * (FX_BM / 4); e += blockDim.x) {
+        const int i = e % my_rows, c4 = e / my_rows;
         const int nl = lo + i;
-        if (n0 + nl >= p.N || m >= p.M) continue;
-        const int col = (m + nl) & (FX_BM - 1);
-        float v = recv[i * FX_BM + col];
-        for (int k = 1; k < ks; ++k) v += recv[(k * my_rows + i) * FX_BM + col];
-        store_y(p.y, static_cast<size_t>(m) * p.N + n0 + nl, v, p.ybf16);
+        const float *src = red + nl * FX_RED_LD + 4 * c4;
+        float4 part[FX_MAX_KS];
+#pragma unroll
+        for (int k = 0; k < FX_MAX_KS; ++k)
+          if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
+        float4 v = part[0];
+#pragma unroll
+        for (int k = 1; k < FX_MAX_KS; ++k)
+          if (k < ks) {
+            v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
+          }
+        if (n0 + nl >= p.N) continue;
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int m = 4 * c4 + t;
+          if (m < p.M) store_y(p.y, static_cast<size_t>(m) * p.N + n0 + nl, vv[t], p.ybf16);
+        }
       }
     }
-    // no CTA leaves while its shared memory may still be copied from
+    // no CTA leaves while its shared memory may still be read
     cluster_sync_all();
   }
   if (warp == 1) {
