@@ -22,8 +22,10 @@
 // Tile: 128 weight rows x 64 tokens; K is split over a cluster of up to 4
 // CTAs exactly as in the bf16 small-M kernel, whose cluster reduction this
 // kernel reuses. Stage = 64 columns (two groups):
-//   A   16 KB  (nib - 8) in bf16, canonical K-major 128-byte swizzle
-//   B   3 x 8 KB  the activation pieces, same layout
+//   A   (nib - 8) in bf16, 128 TMEM lanes x 32 columns (tcgen05.st by the
+//       dequantisers; the MMAs read A from tensor memory, so it costs no
+//       shared-memory bandwidth)
+//   B   3 x 8 KB  the activation pieces, canonical K-major 128-byte swizzle
 // in a ring of 4 MMA stages, and the fp32 activation tiles (16 KB, loaded
 // by TMA as two 128-byte-swizzled halves) in a separate ring of 3 that the
 // dequantisers release as soon as they have split a tile, so activation
@@ -35,7 +37,9 @@
 // Warp roles (448 threads, one CTA per SM):
 //   warp 0       TMA of the fp32 activation tiles;
 //   warp 1       TMEM owner and MMA issuer;
-//   warps 2-9    dequantisers: (nib - 8) tiles of A and the three pieces of B;
+//   warps 2-9    dequantisers: (nib - 8) tiles of A (warp w: TMEM lane
+//                quadrant w % 4, half (w - 2) / 4 of each stage's words)
+//                and the three pieces of B;
 //   warps 10-13  readback: TMEM lanes of one quadrant each, scale, accumulate,
 //                and at the end the partial tile for the cluster reduction.
 // Every wait is bounded; a timeout is recorded and the CTA unwinds.
@@ -65,16 +69,17 @@ constexpr int FX_ROWS = 128;       // weight rows per tile (the MMA M)
 constexpr int FX_DQ_WARPS = 8;
 constexpr int FX_RB_WARPS = 4;
 constexpr int FX_THREADS = 64 + 32 * (FX_DQ_WARPS + FX_RB_WARPS);
-constexpr int FX_A_BYTES = FX_ROWS * FX_BK * 2;  // 16 KB
 constexpr int FX_B_BYTES = FX_BM * FX_BK * 2;    // 8 KB per piece
 constexpr int FX_X_BYTES = FX_BM * FX_BK * 4;    // 16 KB
-constexpr int FX_STAGE = FX_A_BYTES + 3 * FX_B_BYTES;  // one MMA stage
+constexpr int FX_STAGE = 3 * FX_B_BYTES;        // one MMA stage in shared memory (B)
 constexpr int FX_NS = 4;            // MMA stages
 constexpr int FX_NSX = 3;           // fp32 activation tiles in flight
 constexpr int FX_PD = 2;            // stages of packed weights prefetched per thread
 constexpr int FX_NB = 3 * FX_BM;    // MMA N: the three activation pieces side by side
 constexpr int FX_ACC = 2;           // group accumulators in TMEM (FX_NB columns each)
-constexpr int FX_TMEM_COLS = 512;   // FX_ACC * FX_NB rounded up to a power of two
+constexpr int FX_TMEM_COLS = 512;   // the accumulators, then the A ring
+constexpr int FX_A_COL0 = FX_ACC * FX_NB;  // A stage s at column FX_A_COL0 + 32 s
+static_assert(FX_A_COL0 + FX_NS * 32 <= FX_TMEM_COLS, "TMEM budget");
 constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + 1024 + 256;
 constexpr int FX_RED_LD = FX_BM + 4;  // row stride of the parked partial tile (floats)
 constexpr int FX_MAX_KS = 4;          // largest cluster (K split)
@@ -233,8 +238,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
         const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
         if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); break; }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + s * SB);
-        const uint32_t b0 = a0 + FX_A_BYTES;
+        const uint32_t a0 = tmem + FX_A_COL0 + s * 32;  // (nib - 8) in TMEM
+        const uint32_t b0 = smem_u32(smem + s * SB);
         const int groups = min(2, G32 - 2 * kb);  // the last stage may hold one group
         bool ok = true;
         for (int h = 0; h < groups; ++h, ++g) {
@@ -249,8 +254,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
           // one MMA per 16 columns covers the three pieces: A is read once
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            tc_mma(tmem + buf * FX_NB, sw128_desc(a0 + (2 * h + k) * 32),
-                   sw128_desc(b0 + (2 * h + k) * 32), FX_IDESC, k > 0 ? 1u : 0u);
+            tc_mma_tmem_a(tmem + buf * FX_NB, a0 + (2 * h + k) * 8,
+                          sw128_desc(b0 + (2 * h + k) * 32), FX_IDESC, k > 0 ? 1u : 0u);
           tc_commit(&acc_full[buf]);
           issued_any = true;
         }
@@ -268,7 +273,11 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
     const uint32_t magic = opaque_u32(0x43004300u);  // bf16 pair (128, 128)
     const uint32_t bias = opaque_u32(0x43084308u);   // bf16 pair (136, 136)
     const int dq = threadIdx.x - 64;                  // 0 .. 255
-    const int arow = dq >> 1, apart = dq & 1;         // A: row, half of the stage's 8 words
+    // A: TMEM lane = weight row; warp w may only reach lane quadrant w % 4,
+    // so warp w takes row (w % 4) * 32 + lane and half (w - 2) / 4 of the
+    // stage's 8 words
+    const int arow = (warp & 3) * 32 + lane, apart = (warp - 2) >> 2;
+    const uint32_t alane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const int n = n0 + arow;
     const bool nvalid = n < p.N;
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.qw) + static_cast<size_t>(n) * Kw;
@@ -312,10 +321,16 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
           got = mbar_wait(&empty[s], ph ^ 1u) && mbar_wait(&xfull[xs], xph) && !aborted(abort_flag);
         if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { fail(); ok = false; break; }
         uint8_t *st = smem + s * SB;
+        {
+          tc_fence_after();  // the MMAs that read this A stage are complete
+          uint32_t a[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4 *>(st + sw128_offset(arow, apart * 4 + i)) =
-              dequant_word_int(cw[i], magic, bias);
+          for (int i = 0; i < 4; ++i) {
+            const uint4 d = dequant_word_int(cw[i], magic, bias);
+            a[4 * i] = d.x; a[4 * i + 1] = d.y; a[4 * i + 2] = d.z; a[4 * i + 3] = d.w;
+          }
+          tmem_st_16cols(alane + FX_A_COL0 + s * 32 + apart * 16, a);
+        }
         // the fp32 tile: two [64 tokens][32 columns] halves, 16-byte pieces
         // of each 128-byte row swizzled by the row index
         const uint8_t *xt = xring + xs * FX_X_BYTES;
@@ -330,10 +345,12 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
           uint4 o1, o2, o3;
           split_chunk(v, o1, o2, o3);
           const uint32_t off = sw128_offset(bm, chunk);
-          *reinterpret_cast<uint4 *>(st + FX_A_BYTES + off) = o1;
-          *reinterpret_cast<uint4 *>(st + FX_A_BYTES + FX_B_BYTES + off) = o2;
-          *reinterpret_cast<uint4 *>(st + FX_A_BYTES + 2 * FX_B_BYTES + off) = o3;
+          *reinterpret_cast<uint4 *>(st + off) = o1;
+          *reinterpret_cast<uint4 *>(st + FX_B_BYTES + off) = o2;
+          *reinterpret_cast<uint4 *>(st + 2 * FX_B_BYTES + off) = o3;
         }
+        tmem_store_wait();
+        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
