@@ -20,8 +20,12 @@
 //                (M=128, N=64, K=16) with A from TMEM, one commit;
 //   warps 2-17   dequantisers: warp w handles block (w - 2) / 4 of every
 //                stage for TMEM lane quadrant w % 4; thread = weight row,
-//                8 packed words (64 columns) per block, dequantised to
-//                bf16 pairs and stored as 32 TMEM columns.
+//                8 packed words (64 columns) per block, read from the
+//                weight ring, dequantised to bf16 pairs and stored as 32
+//                TMEM columns;
+//   warp 18      weight producer: one TMA box of the stage's packed words
+//                (128 rows x 128 bytes, 128-byte swizzle) into a ring of 4,
+//                so the weight stream runs ahead with few, large requests.
 // TMEM: columns 0-63 the fp32 accumulator, 64 + 32 * (stage * 4 + block)
 // the A blocks (448 of 512 columns).
 // Epilogue: each rank parks its fp32 partial tile in shared memory; after a
@@ -55,13 +59,17 @@ constexpr int SP_BK = 64;          // K columns per block
 constexpr int SP_SK = 4;           // blocks per stage
 constexpr int SP_NS = 3;           // stages
 constexpr int SP_DQ_WARPS = 16;    // 4 blocks x 4 lane quadrants
-constexpr int SP_THREADS = 64 + 32 * SP_DQ_WARPS;
+constexpr int SP_WP_WARP = 2 + SP_DQ_WARPS;  // the weight producer (TMA)
+constexpr int SP_THREADS = 96 + 32 * SP_DQ_WARPS;
+constexpr int SP_NW = 4;           // stages of packed weights in shared memory
+constexpr int SP_W_BYTES = SP_ROWS * SP_SK * 32;  // 128 rows x 128 B per stage
 constexpr int SP_B_BYTES = SP_BM * SP_BK * 2;               // 8 KB per block
 constexpr int SP_ACC_COLS = SP_BM;                          // fp32 accumulator
 constexpr int SP_A_COL0 = SP_ACC_COLS;                      // first A block column
 constexpr int SP_TMEM_COLS = 512;
 constexpr int SP_RING_BYTES = SP_NS * SP_SK * SP_B_BYTES;   // 96 KB
-constexpr int SP_SMEM = SP_RING_BYTES + 1024 + 256;
+constexpr int SP_WRING_BYTES = SP_NW * SP_W_BYTES;         // 64 KB
+constexpr int SP_SMEM = SP_RING_BYTES + SP_WRING_BYTES + 1024 + 256;
 constexpr int SP_RED_LD = SP_BM + 4;  // row stride of the parked partial tile (floats)
 constexpr int SP_MAX_KS = 8;          // largest cluster (K split)
 static_assert(SP_A_COL0 + SP_NS * SP_SK * 32 <= SP_TMEM_COLS, "TMEM budget");
@@ -85,13 +93,17 @@ struct SpParams {
 };
 
 __global__ void __launch_bounds__(SP_THREADS, 1)
-    tc_split_kernel(const __grid_constant__ CUtensorMap tmap_x, const SpParams p) {
+    tc_split_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                    const __grid_constant__ CUtensorMap tmap_w, const SpParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SP_RING_BYTES);
+  uint8_t *wring = smem + SP_RING_BYTES;  // packed weights, 128-byte swizzle
+  uint64_t *full = reinterpret_cast<uint64_t *>(wring + SP_WRING_BYTES);
   uint64_t *empty = full + SP_NS;
-  uint64_t *acc_full = empty + SP_NS;
+  uint64_t *wfull = empty + SP_NS;     // [SP_NW] packed weights landed
+  uint64_t *wempty = wfull + SP_NW;    // [SP_NW] packed weights read
+  uint64_t *acc_full = wempty + SP_NW;
   uint64_t *drain = acc_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -112,6 +124,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     for (int s = 0; s < SP_NS; ++s) {
       mbar_init(&full[s], 1 + SP_DQ_WARPS);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < SP_NW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], SP_DQ_WARPS);
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
@@ -184,6 +200,21 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         mbar_wait(drain, 0);
       }
     }
+  } else if (warp == SP_WP_WARP) {
+    // ------------------------------------------------- weight producer (TMA)
+    // one 128-row x 32-word box per stage (the 4 blocks' packed words;
+    // words past K read as zero), 128-byte swizzle; runs SP_NW stages ahead
+    if (lane == 0) {
+      int it = 0;
+      for (int kb = kb0; kb < kb1 && !aborted(abort_flag); kb += SP_SK, ++it) {
+        const int ws = it % SP_NW;
+        const uint32_t ph = static_cast<uint32_t>(it / SP_NW) & 1u;
+        if (!mbar_wait(&wempty[ws], ph ^ 1u)) { fail(); break; }
+        if (aborted(abort_flag)) break;
+        mbar_arrive_expect_tx(&wfull[ws], SP_W_BYTES);
+        tma_load_2d(wring + ws * SP_W_BYTES, &tmap_w, kb * 8, n0, &wfull[ws]);
+      }
+    }
   } else {
     // ---------------------------------------------------- dequantisers
     const NibbleConsts nk_ = make_nibble_consts();
@@ -195,30 +226,26 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const bool nvalid = n < p.N;
     const int Kw = K >> 3;
     const int G = K >> p.gs;
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.qw) +
-                           static_cast<size_t>(nvalid ? n : 0) * Kw;
     const float *srow = p.sc + static_cast<size_t>(nvalid ? n : 0) * G;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-
-    // the 8 packed words (2 x 16 B) and 2 scales of this row in block kb
-    auto fetch = [&](int kb, uint4 (&w)[2], float (&sc)[2]) {
-      w[0] = w[1] = make_uint4(0, 0, 0, 0);
+    // this row's two scales of block kb (0 past K or N)
+    auto fetch_sc = [&](int kb, float (&sc)[2]) {
       sc[0] = sc[1] = 0.f;
       if (!nvalid || kb >= kb1) return;
-      const int w0 = kb * 8;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (w0 + 4 * h < Kw) {
-          w[h] = __ldg(reinterpret_cast<const uint4 *>(qrow + w0 + 4 * h));
-          sc[h] = __ldg(srow + (((w0 + 4 * h) * 8) >> p.gs));  // 32 columns, one group
-        }
+        const int w0 = kb * 8 + 4 * h;
+        if (w0 < Kw) sc[h] = __ldg(srow + ((w0 * 8) >> p.gs));  // 32 columns, one group
       }
     };
-    // two stages of this warp's block in flight
-    uint4 rw[2][2];
+    // this row's 16-byte chunks 2j and 2j+1 in a weight stage (row r at
+    // r * 128 bytes, chunk c at (c ^ (r & 7)) * 16)
+    const uint32_t wsw = static_cast<uint32_t>(row & 7);
+    const uint32_t woff0 = static_cast<uint32_t>(row * 128) + (((2u * j) ^ wsw) << 4);
+    const uint32_t woff1 = static_cast<uint32_t>(row * 128) + (((2u * j + 1u) ^ wsw) << 4);
     float rsc[2][2];
-    fetch(kb0 + j, rw[0], rsc[0]);
-    fetch(kb0 + SP_SK + j, rw[1], rsc[1]);
+    fetch_sc(kb0 + j, rsc[0]);
+    fetch_sc(kb0 + SP_SK + j, rsc[1]);
     int it = 0;
     bool ok = true;
     for (int kbase = kb0; kbase < kb1 && ok; kbase += 2 * SP_SK) {
@@ -226,20 +253,24 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       for (int u = 0; u < 2; ++u) {
         const int kbs = kbase + u * SP_SK;  // first block of the stage
         if (kbs >= kb1) break;
-        const int s = it % SP_NS;
+        const int s = it % SP_NS, ws = it % SP_NW;
         const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
+        const uint32_t wph = static_cast<uint32_t>(it / SP_NW) & 1u;
         ++it;
-        const uint4 cw[2] = {rw[u][0], rw[u][1]};
         const float cs[2] = {rsc[u][0], rsc[u][1]};
-        fetch(kbs + 2 * SP_SK + j, rw[u], rsc[u]);
-        const bool got =
-            __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
+        fetch_sc(kbs + 2 * SP_SK + j, rsc[u]);
+        // the packed words have landed, then the TMEM slot is free
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&wfull[ws], wph) &&
+                                                     mbar_wait(&empty[s], ph ^ 1u) &&
+                                                     !aborted(abort_flag));
         if (!got) { fail(); ok = false; break; }
+        const uint8_t *wst = wring + ws * SP_W_BYTES;
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(wst + woff0);
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(wst + woff1);
         tc_fence_after();
         if (kbs + j < kb1) {
           uint32_t a[32];
-          const uint32_t wv[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w,
-                                  cw[1].x, cw[1].y, cw[1].z, cw[1].w};
+          const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint4 d = dequant_word(wv[i], cs[i >> 2], nk_);
@@ -248,6 +279,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           tmem_st_32cols(lane_base + SP_A_COL0 + (s * SP_SK + j) * 32, a);
           tmem_store_wait();
         }
+        // the words were consumed above: release the weight slot
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[ws]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[s]);
@@ -342,6 +376,16 @@ cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *s
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // packed weights [N][K/8] words: one 32-word (128-byte) x 128-row box per
+  // stage, 128-byte swizzle, zeros past K and N
+  CUtensorMap tmap_w;
+  const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
+  const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
+  const cuuint32_t wbox[2] = {SP_SK * 8, SP_ROWS};
+  r = encode(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<int32_t *>(qw), wdims, wstrides,
+             wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   SpParams p{};
   p.qw = qw;
   p.sc = sc;
@@ -383,7 +427,7 @@ cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *s
   attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, p);
 }
 
 }  // namespace w4a16
