@@ -470,12 +470,20 @@ def dist_env():
 
 
 def reduce_max(torch, value, world):
+    """Max of `value` over the ranks (the slowest replica sets the time)."""
     if world == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(world, units_per_rank_step, max_seconds_per_step):
+    """Whole-job rate: every rank's units of one step over the slowest rank's
+    time (replicas: per-rank work is fixed as N grows, "weak" scaling)."""
+    return world * units_per_rank_step / max_seconds_per_step
 
 
 def barrier(world):
@@ -577,10 +585,7 @@ def run_ours(args):
         raise RuntimeError(f"device status after the timed region: {w4.status_string(status)}")
 
     per_step_s = ms / 1e3 / args.steps
-    if wl.unit == "TFLOP/s":
-        value = world * wl.flops / per_step_s / 1e12
-    else:
-        value = world * wl.bytes / per_step_s / 1e12
+    value = aggregate_rate(world, wl.flops if wl.unit == "TFLOP/s" else wl.bytes, per_step_s) / 1e12
 
     # end to end through the public API, host buffers in and out each step
     e2e_steps = min(args.steps, args.e2e_steps)
@@ -593,7 +598,7 @@ def run_ours(args):
         t_e2e = time.perf_counter() - t0
     t_e2e = reduce_max(torch, t_e2e, world)
     per_e2e = t_e2e / e2e_steps
-    e2e_value = world * (wl.flops if wl.unit == "TFLOP/s" else wl.bytes) / per_e2e / 1e12
+    e2e_value = aggregate_rate(world, wl.flops if wl.unit == "TFLOP/s" else wl.bytes, per_e2e) / 1e12
 
     # roofline of the dominant kernel (the only kernel of the decode step)
     per_launch_s = per_step_s / wl.kernels_per_step
