@@ -44,24 +44,6 @@ __device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t 
       : "memory");
 }
 
-// Distributed shared memory: the address of the same variable in the CTA
-// of cluster rank `rank`.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-// Bulk copy from this CTA's shared memory into a (possibly remote) CTA's
-// shared memory in the cluster, completing on that CTA's mbarrier.
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void *src,
-                                               uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
