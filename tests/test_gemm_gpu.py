@@ -404,3 +404,50 @@ def test_bf16_output_needs_a_bf16_buffer(w4):
     sc = torch.zeros((8, 2), dtype=torch.float32, device="cuda")
     with pytest.raises(TypeError):
         w4.w4a16_gemm(x, qw, sc, y=torch.zeros((1, 8), device="cuda"), out_dtype="bf16")
+
+
+# The bench's launch configuration: programmatic launch (overlap) inside one
+# CUDA graph replayed on a side stream, back-to-back calls on rotating weight
+# copies. Every call's output must match the oracle as in eager mode.
+@pytest.mark.parametrize("M,N,K,dt", [
+    (1, 4096, 7168, "f32"),      # decode GEMV: streaming kernel
+    (64, 4096, 7168, "bf16"),    # tree-verify gate/up: small-M tensor-core kernel
+    (64, 7168, 2048, "f32"),     # tree-verify down: fp32-exact tensor-core kernel
+])
+def test_graph_replay_with_overlap_matches_oracle(w4, M, N, K, dt):
+    ncopies = 3
+    x = synth.activations(40 + M, M, K, outlier_frac=0.01 if M > 1 else 0.0)
+    xt = torch.from_numpy(x)
+    if dt == "bf16":
+        xt = xt.to(torch.bfloat16)
+    xd = xt.cuda()
+    host, dev = [], []
+    for c in range(ncopies):
+        w = synth.weights(40 + M, N, K, sub=c)
+        qw_d, sc_d, qw_h, sc_h = quantize_both(w4, w)
+        host.append((qw_h, sc_h))
+        dev.append((qw_d, sc_d))
+    ys = [torch.full((M, N), float("nan"), device="cuda") for _ in range(2 * ncopies)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(2):  # warm-up outside the graph
+            w4.w4a16_gemm(xd, *dev[i % ncopies], y=ys[i], overlap=True, stream=stream)
+    stream.synchronize()
+    for y in ys:
+        y.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(2 * ncopies):
+            w4.w4a16_gemm(xd, *dev[i % ncopies], y=ys[i], overlap=True,
+                          stream=torch.cuda.current_stream())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    xo = xt.float().numpy()
+    for c in range(ncopies):
+        ref, bound = oracle.gemm_ref(xo, *host[c])
+        for y in (ys[c], ys[c + ncopies]):
+            err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+            assert np.all(err <= TOL[dt] * bound), f"copy {c}: max err/bound {np.max(err / bound):.3e}"
+        assert torch.equal(ys[c].view(torch.int32), ys[c + ncopies].view(torch.int32))
