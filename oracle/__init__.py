@@ -39,10 +39,10 @@ Readings where the pages are silent (each is listed in the design notes):
     GEMM consumes), y[t] = sum over the token's k slots, in slot order, of
     route_w * (h @ W_down^T).
 
-  * MoE routing (the "DeepSeekV3/Kimi-style ... MoE routing with shared
-    expert" of [QC] "The Context: A Native DDTree Engine Takes Shape" and
-    [PC] "The Context: Phase 3 of a Custom Inference Stack"; the pages give
-    no formula, so the published DeepSeek-V3 gate is taken): fp32 router
+  * MoE routing (a DeepSeekV3/Kimi-style MoE whose routing includes a shared
+    expert: [QC] "The Context: A Native DDTree Engine Takes Shape" and [PC]
+    "The Context: Phase 3 of a Custom Inference Stack"; the pages give no
+    formula, so the published DeepSeek-V3 gate is taken): fp32 router
     logits l = x @ W_r^T, scores s = sigmoid(l), the k experts with the
     largest s + b (b an optional per-expert selection bias; equal values go
     to the lower expert id), weights s_j / sum of the k chosen s times a
