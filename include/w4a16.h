@@ -16,8 +16,9 @@
  *   W_hat[n][k] = (nibble(n,k) - 8) * sc[n][k/group]
  *
  * Operation. "The Silence of Success: A Single Line That Speaks Volumes",
- * section "What the Edit Actually Built": activations (fp32; a bf16 mode is
- * the "16-bit activations" of the W4A16 name) times the INT4 weights with
+ * section "What the Edit Actually Built": activations (fp32; a bf16 mode
+ * gives the 16-bit activations the W4A16 name stands for) times the INT4
+ * weights with
  * fp32 accumulation:  y[m][n] = sum_k x[m][k] * W_hat[n][k]  ("NT": both
  * operands K-contiguous, y row-major fp32).
  *
