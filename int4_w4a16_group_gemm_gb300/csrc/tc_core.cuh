@@ -105,20 +105,24 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, float s, const NibbleC
   const uint32_t w8 = w >> 8;
   const uint64_t p[4] = {nibble_pair<0>(w, w8, k), nibble_pair<1>(w, w8, k),
                          nibble_pair<2>(w, w8, k), nibble_pair<3>(w, w8, k)};
-  float v[8];
+  // the odd nibble classes carry 16 (n - 8): scale them by s / 16 (exact,
+  // a power-of-two scaling); one packed multiply per nibble pair
+  const float so = s * nibble_prescale(1);
+  uint64_t se2, so2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(se2) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(so2) : "f"(so));
+  float lo[4], hi[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const float sc = s * nibble_prescale(c);  // exact: a power-of-two scaling
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p[c]));
-    v[c] = lo * sc;
-    v[4 + c] = hi * sc;
+    uint64_t v;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(v) : "l"(p[c]), "l"((c & 1) ? so2 : se2));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo[c]), "=f"(hi[c]) : "l"(v));
   }
   uint4 o;
-  o.x = pack_bf16x2(v[0], v[1]);
-  o.y = pack_bf16x2(v[2], v[3]);
-  o.z = pack_bf16x2(v[4], v[5]);
-  o.w = pack_bf16x2(v[6], v[7]);
+  o.x = pack_bf16x2(lo[0], lo[1]);
+  o.y = pack_bf16x2(lo[2], lo[3]);
+  o.z = pack_bf16x2(hi[0], hi[1]);
+  o.w = pack_bf16x2(hi[2], hi[3]);
   return o;
 }
 
