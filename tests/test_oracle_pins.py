@@ -587,3 +587,22 @@ def test_moe_block_shared_expert_closed_forms():
     # linearity in the routed part: block = routed layer + shared alone
     y3, _ = oracle.moe_block_ref(x, ids, rw, qgu, sgu, qdn, sdn, shared, False, 1e-5)
     np.testing.assert_allclose(y3, base + y2, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_block_bf16_mode_is_routed_layer_plus_shared_expert():
+    """In bf16 mode each expert rounds its own h to bf16, so the block is still
+    the routed layer plus the shared expert alone (run as a top-1 layer with
+    unit weight), and the bound adds up the same way."""
+    T, H, I, Is, E, topk = 4, 64, 32, 64, 5, 3
+    x = oracle.round_to_bf16(synth.activations(41, T, H))
+    ids, rw = synth.routing(41, T, topk, E)
+    qgu, sgu, qdn, sdn = _small_experts(41, E, H, I)
+    a, b = oracle.quantize_w4a16(synth.weights(42, 2 * Is, H))
+    c, d = oracle.quantize_w4a16(synth.weights(43, H, Is))
+    yb, tb = oracle.moe_block_ref(x, ids, rw, qgu, sgu, qdn, sdn, (a, b, c, d), True, 4e-3)
+    yr, tr = oracle.moe_ref(x, ids, rw, qgu, sgu, qdn, sdn, True, 4e-3)
+    ys, ts = oracle.moe_ref(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32),
+                            a[None], b[None], c[None], d[None], True, 4e-3)
+    np.testing.assert_allclose(yb, yr + ys, rtol=1e-12, atol=1e-12)
+    # the block's bound covers both parts (slot-sum term grows by one slot)
+    assert np.all(tb >= tr + ts - 1e-12 * (np.abs(yr) + np.abs(ys)))
