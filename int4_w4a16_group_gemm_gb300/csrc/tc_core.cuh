@@ -177,6 +177,42 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(const float *p, uint32_t rank
   return v;
 }
 
+// Split-K reduction by the owner of a row slice. Every CTA of the cluster
+// has parked its fp32 partial tile at red[row * LD + column] (BM columns) in
+// its shared memory and passed a cluster barrier. This CTA owns rows
+// lo .. lo + my_rows - 1: it reads 4 columns of a row from every rank
+// (16-byte distributed shared-memory loads, all issued before the sums),
+// adds them in rank order and stores y[m0 + m][n0 + row] for m0 + m < M and
+// n0 + row < N. Consecutive threads take consecutive rows, so the y stores
+// coalesce.
+template <int BM, int LD, int MAXKS>
+__device__ __forceinline__ void split_k_owner_reduce(const float *red, int lo, int my_rows, int ks,
+                                                     int n0, int m0, int M, int N, void *y,
+                                                     int ybf16) {
+  for (int e = threadIdx.x; e < my_rows * (BM / 4); e += blockDim.x) {
+    const int i = e % my_rows, c4 = e / my_rows;
+    const int nl = lo + i;
+    const float *src = red + nl * LD + 4 * c4;
+    float4 part[MAXKS];
+#pragma unroll
+    for (int k = 0; k < MAXKS; ++k)
+      if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
+    float4 v = part[0];
+#pragma unroll
+    for (int k = 1; k < MAXKS; ++k)
+      if (k < ks) {
+        v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
+      }
+    if (n0 + nl >= N) continue;
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int m = 4 * c4 + t;
+      if (m0 + m < M) store_y(y, static_cast<size_t>(m0 + m) * N + n0 + nl, vv[t], ybf16);
+    }
+  }
+}
+
 __device__ __forceinline__ bool aborted(const int *flag) {
   return *reinterpret_cast<const volatile int *>(flag) != 0;
 }

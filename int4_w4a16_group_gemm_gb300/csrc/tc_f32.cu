@@ -422,35 +422,9 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   {
     const float *red = reinterpret_cast<const float *>(smem);
     const bool ok_here = *reinterpret_cast<volatile int *>(abort_flag) == 0;
-    if (ok_here) {
-      // owner of rows lo .. lo + my_rows - 1: read 4 columns of a row from
-      // every rank (16-byte distributed shared-memory loads, all issued
-      // before the sums) and add them in rank order; consecutive threads
-      // take consecutive rows, so the y stores coalesce
-      const int lo = slice_lo(rank);
-      for (int e = threadIdx.x; e < my_rows * (FX_BM / 4); e += blockDim.x) {
-        const int i = e % my_rows, c4 = e / my_rows;
-        const int nl = lo + i;
-        const float *src = red + nl * FX_RED_LD + 4 * c4;
-        float4 part[FX_MAX_KS];
-#pragma unroll
-        for (int k = 0; k < FX_MAX_KS; ++k)
-          if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
-        float4 v = part[0];
-#pragma unroll
-        for (int k = 1; k < FX_MAX_KS; ++k)
-          if (k < ks) {
-            v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
-          }
-        if (n0 + nl >= p.N) continue;
-        const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int m = 4 * c4 + t;
-          if (m < p.M) store_y(p.y, static_cast<size_t>(m) * p.N + n0 + nl, vv[t], p.ybf16);
-        }
-      }
-    }
+    if (ok_here)
+      split_k_owner_reduce<FX_BM, FX_RED_LD, FX_MAX_KS>(red, slice_lo(rank), my_rows, ks, n0, 0,
+                                                        p.M, p.N, p.y, p.ybf16);
     // no CTA leaves while its shared memory may still be read
     cluster_sync_all();
   }

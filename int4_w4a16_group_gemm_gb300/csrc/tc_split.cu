@@ -319,34 +319,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const bool ok_all = *reinterpret_cast<volatile int *>(abort_flag) == 0;
     const int lo = slice_lo(rank), my_rows = slice_lo(rank + 1) - lo;
     const float *red = reinterpret_cast<const float *>(smem);
-    if (ok_all) {
-      // owner of rows lo .. lo + my_rows - 1: read 4 columns of a row from
-      // every rank (16-byte distributed shared-memory loads, all issued
-      // before the sums) and add them in rank order; consecutive threads
-      // take consecutive rows, so the y stores coalesce
-      for (int e = threadIdx.x; e < my_rows * (SP_BM / 4); e += blockDim.x) {
-        const int i = e % my_rows, c4 = e / my_rows;
-        const int nl = lo + i;
-        const float *src = red + nl * SP_RED_LD + 4 * c4;
-        float4 part[SP_MAX_KS];
-#pragma unroll
-        for (int k = 0; k < SP_MAX_KS; ++k)
-          if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
-        float4 v = part[0];
-#pragma unroll
-        for (int k = 1; k < SP_MAX_KS; ++k)
-          if (k < ks) {
-            v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
-          }
-        if (n0 + nl >= p.N) continue;
-        const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int m = 4 * c4 + t;
-          if (m0 + m < p.M) store_y(p.y, static_cast<size_t>(m0 + m) * p.N + n0 + nl, vv[t], p.ybf16);
-        }
-      }
-    }
+    if (ok_all)
+      split_k_owner_reduce<SP_BM, SP_RED_LD, SP_MAX_KS>(red, lo, my_rows, ks, n0, m0, p.M, p.N,
+                                                        p.y, p.ybf16);
   }
   // no CTA leaves while its shared memory may still be read
   cluster_sync_all();
