@@ -137,3 +137,33 @@ def test_router_and_block_argument_checks_need_no_gpu(w4):
     assert block(64, fake, group=128, H=128, I=128) == w4.W4A16_ERR_INVALID_ARG  # Is % group
     assert block(64, fake, group=16) == w4.W4A16_ERR_UNSUPPORTED
     assert block(64, fake, ws=100) == w4.W4A16_ERR_INVALID_ARG  # workspace too small
+
+
+def test_binding_rejects_host_tensors(w4):
+    """Every step runs in the CUDA kernels: host tensors are refused before
+    any library call, never computed on the CPU."""
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((1, 64), dtype=torch.float32)
+    qw = torch.zeros((8, 8), dtype=torch.int32)
+    sc = torch.zeros((8, 2), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        w4.w4a16_gemm(x, qw, sc)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        w4.w4a16_quantize(torch.zeros((8, 64), dtype=torch.float32))
+    with pytest.raises(TypeError):
+        w4.w4a16_gemm(x.double(), qw, sc)  # neither fp32 nor bf16
+
+
+def test_package_without_library_fails_to_import(tmp_path):
+    """A copy of the package without libw4a16.so raises on import (no fallback)."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "int4_w4a16_group_gemm_gb300")
+    dst = tmp_path / "int4_w4a16_group_gemm_gb300"
+    dst.mkdir()
+    shutil.copy(os.path.join(pkg, "__init__.py"), dst / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import int4_w4a16_group_gemm_gb300"],
+                       cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libw4a16.so" in r.stderr
