@@ -441,7 +441,7 @@ class MoeBlockWorkload(MoeWorkload):
                                           f"({len(experts)} experts + shared), scaled by tokens")
 
 
-def make_workload(cfg, dtype, w4, torch, dev, overlap=True):
+def make_workload(cfg, dtype, w4, torch, dev, overlap=True, moe_experts=384, moe_tokens=128):
     if cfg == 0:
         return GemmWorkload(w4, torch, dev, 1, 512, 256, "f32", 0, "tiny GEMM M=1 K=256 N=512 fp32",
                             overlap=overlap)
@@ -452,12 +452,12 @@ def make_workload(cfg, dtype, w4, torch, dev, overlap=True):
     if cfg == 2:
         return TreeVerifyWorkload(w4, torch, dev, dtype)
     if cfg == 3:
-        return MoeWorkload(w4, torch, dev)
+        return MoeWorkload(w4, torch, dev, T=moe_tokens, E=moe_experts)
     if cfg == 4:
         return GemmWorkload(w4, torch, dev, 2048, 18432, 7168, "bf16", 0,
                             "prefill GEMM M=2048 K=7168 N=18432 bf16")
     if cfg == 5:
-        return MoeBlockWorkload(w4, torch, dev)
+        return MoeBlockWorkload(w4, torch, dev, T=moe_tokens, E=moe_experts)
     raise ValueError(cfg)
 
 
@@ -501,7 +501,8 @@ def run_reference(args):
     import torch
     import int4_w4a16_group_gemm_gb300 as w4
     dev = torch.device("cuda", 0)
-    wl = make_workload(args.config, args.dtype, w4, torch, dev)
+    wl = make_workload(args.config, args.dtype, w4, torch, dev, moe_experts=args.moe_experts,
+                       moe_tokens=args.moe_tokens)
     budget = max(0.02, min(5.0, 90.0 / max(1, args.steps + args.warmup)))
     vals = []
     desc = ""
@@ -538,7 +539,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     import int4_w4a16_group_gemm_gb300 as w4
 
-    wl = make_workload(args.config, args.dtype, w4, torch, dev, overlap=not args.no_overlap)
+    wl = make_workload(args.config, args.dtype, w4, torch, dev, overlap=not args.no_overlap,
+                       moe_experts=args.moe_experts, moe_tokens=args.moe_tokens)
     stream = torch.cuda.Stream(device=dev)
     pk = peaks()
 
@@ -669,6 +671,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--moe-experts", type=int, default=384,
+                    help="experts of the MoE workloads (configs 3 and 5); fewer only to profile "
+                         "the same kernels on a smaller working set")
+    ap.add_argument("--moe-tokens", type=int, default=128,
+                    help="tokens of the MoE workloads (configs 3 and 5); see --moe-experts")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
