@@ -195,6 +195,60 @@ def _silu_slope_max() -> float:
     return 1.1
 
 
+def _swiglu_one(wgu, xt, eps, slope):
+    """Exact SwiGLU of one token through one expert (wgu dequantised, fp64)
+    and the bound dh on |h_impl - h| for an implementation whose gate/up GEMM
+    stays within eps * sum|x * w| and which evaluates silu and the product in
+    fp32 (first-order propagation through SwiGLU)."""
+    I = wgu.shape[0] // 2
+    gu = wgu @ xt
+    bgu = np.abs(wgu) @ np.abs(xt)
+    g, u = gu[:I], gu[I:]
+    dg, du = eps * bgu[:I], eps * bgu[I:]
+    h = silu(g) * u
+    dh = slope * (np.abs(u) + du) * dg + np.abs(silu(g)) * du + 4e-7 * np.abs(h)
+    return h, dh
+
+
+def moe_swiglu_ref(x, qw_gu, sc_gu, bf16_mode: bool, eps: float, group: int = GROUP):
+    """The gate/up GEMM and SwiGLU of ONE expert for tokens x[m, H].
+
+    [QC] "The Context: A Native DDTree Engine Takes Shape" (SwiGLU between
+    the expert GEMMs): [g; u] = x @ W_hat_gu^T, h = silu(g) * u.
+    Returns (h, tol): h [m, I] exact in fp64, and tol [m, I] such that an
+    implementation whose gate/up GEMM stays within eps * sum|x * w|, which
+    evaluates silu and the product in fp32 and, in bf16 mode, stores h
+    rounded to bf16 (nearest, 2^-9 relative), is within tol of h.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    wgu = dequantize(qw_gu, sc_gu, group).astype(np.float64)
+    I = wgu.shape[0] // 2
+    h = np.zeros((x.shape[0], I))
+    tol = np.zeros((x.shape[0], I))
+    for m in range(x.shape[0]):
+        h[m], dh = _swiglu_one(wgu, x[m].astype(np.float64), eps, _silu_slope_max())
+        tol[m] = dh * (1 + 2.0 ** -9) + 2.0 ** -9 * np.abs(h[m]) if bf16_mode else dh
+    return h, tol
+
+
+def moe_down_ref(h_in, route_w, qw_dn, sc_dn, eps: float, group: int = GROUP):
+    """The down GEMM of ONE expert fed the given h, times the routing weight.
+
+    [QC] "The Context: A Native DDTree Engine Takes Shape" (the down
+    projection after SwiGLU); the routing weight scales each slot's output.
+    o[m] = route_w[m] * (h_in[m] @ W_hat_dn^T), exact in fp64. Returns
+    (o, tol): tol = |route_w| * eps * (|h_in| @ |W_hat_dn|^T) (a GEMM within
+    eps of sum|h * w|) plus 2^-23 |o| (the fp32 product by the routing
+    weight and its rounding).
+    """
+    h_in = np.asarray(h_in, dtype=np.float64)
+    r = np.asarray(route_w, dtype=np.float32).astype(np.float64)
+    wdn = dequantize(qw_dn, sc_dn, group).astype(np.float64)
+    o = r[:, None] * (h_in @ wdn.T)
+    tol = np.abs(r)[:, None] * eps * (np.abs(h_in) @ np.abs(wdn).T) + 2.0 ** -23 * np.abs(o)
+    return o, tol
+
+
 def moe_ref(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, bf16_mode: bool,
             eps: float, group: int = GROUP, tokens=None):
     """Grouped MoE layer: y[t] = sum_slot r[t,slot] * (h @ W_dn[e]^T).
@@ -232,17 +286,8 @@ def moe_ref(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, bf16_mode: bool,
     for e in sorted(by_expert):
         wgu = dequantize(qw_gu[e], sc_gu[e], group).astype(np.float64)
         wdn = dequantize(qw_dn[e], sc_dn[e], group).astype(np.float64)
-        I = wgu.shape[0] // 2
         for (t, j) in by_expert[e]:
-            xt = x[t].astype(np.float64)
-            gu = wgu @ xt
-            bgu = np.abs(wgu) @ np.abs(xt)
-            g, u = gu[:I], gu[I:]
-            dg, du = eps * bgu[:I], eps * bgu[I:]
-            h = silu(g) * u
-            # first-order propagation of the gate/up errors through SwiGLU,
-            # plus the fp32 evaluation of silu and of the product
-            dh = slope * (np.abs(u) + du) * dg + np.abs(silu(g)) * du + 4e-7 * np.abs(h)
+            h, dh = _swiglu_one(wgu, x[t].astype(np.float64), eps, slope)
             if bf16_mode:
                 h_in = round_to_bf16(h.astype(np.float32)).astype(np.float64)
                 # both sides round h to bf16: a rounding flip costs up to one
