@@ -72,11 +72,19 @@ typedef enum {
 /* Kernel choice for w4a16_gemm_ex (tests and tuning). */
 typedef enum {
   W4A16_ALGO_AUTO = 0,   /* pick by M and dtype (what w4a16_gemm does) */
-  W4A16_ALGO_SIMT = 1,   /* streaming CUDA-core kernel, any M, both dtypes */
-  W4A16_ALGO_TC = 2      /* tcgen05 tensor-core kernel: bf16 activations, or
+  W4A16_ALGO_SIMT = 1,   /* the streaming CUDA-core kernel, any M, both
+                            dtypes (same as W4A16_ALGO_STREAM) */
+  W4A16_ALGO_TC = 2,     /* tcgen05 tensor-core kernel: bf16 activations, or
                             fp32 activations with M <= 64 and K <= 16384
                             (each activation split exactly into three bf16
                             pieces, group scales applied in fp32) */
+  W4A16_ALGO_STREAM = 3, /* the streaming CUDA-core kernel (token tiles of
+                            up to 3), any M, K <= 16384 */
+  W4A16_ALGO_GEMV = 4    /* the decode GEMV kernel: M = 1, K <= 8192 and
+                            K/group a multiple of 4 (UNSUPPORTED otherwise).
+                            One CTA per SM, sized so that under
+                            W4A16_FLAG_OVERLAP the next call's CTA streams
+                            its weights into shared memory beside it */
 } w4a16_algo;
 
 /*
@@ -165,6 +173,21 @@ w4a16_status w4a16_moe_sort(const int32_t *expert_ids, int n_pairs, int E,
 /* Bytes of workspace w4a16_moe_gemm needs for these sizes (either dtype). */
 size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I);
 
+/* Where w4a16_moe_gemm leaves its intermediates in the workspace, for
+ * inspection (per-stage checks and debugging); host-only. After a call
+ * with these sizes the workspace holds, at the returned byte offsets:
+ *   off_perm: perm [T*topk] int32, the pairs p = t*topk + slot in expert
+ *             order (as w4a16_moe_sort returns it);
+ *   off_h:    h [T*topk][I], row s = the SwiGLU output silu(g)*u of pair
+ *             perm[s] - bf16 elements in bf16 mode, fp32 otherwise;
+ *   off_o:    o [T*topk][H] fp32, row p = route_w[p] * (h @ W_hat_dn^T)
+ *             of pair p (before the slot sum).
+ * The same offsets hold for w4a16_moe_block, whose routed layer starts at
+ * byte 0 of its workspace.
+ * Errors: INVALID_ARG (non-positive size, null output pointer). */
+w4a16_status w4a16_moe_workspace_layout(int T, int topk, int E, int H, int I,
+                                        size_t *off_perm, size_t *off_h, size_t *off_o);
+
 /*
  * w4a16_moe_gemm - a grouped MoE layer on INT4 experts ("The Quiet Commit:
  * ... Major Engineering Milestone", section "The Context: A Native DDTree
@@ -215,6 +238,8 @@ w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt,
  *   - Every call shares the one array and leaves its contents behind; no
  *     intermediate needs to start at zero. Calls that overlap on the GPU
  *     (other streams, other host threads) race on it: order them.
+ *   - The array used is the current device's: every pointer passed must be
+ *     memory of the device that is current when the call is made.
  * Errors: as w4a16_moe_gemm, plus UNSUPPORTED for sizes beyond the array.
  */
 w4a16_status w4a16_moe_gemm_noalloc(const void *x, w4a16_act_dtype xdt,
@@ -287,8 +312,8 @@ w4a16_status w4a16_moe_block(const void *x, w4a16_act_dtype xdt, int T,
                              w4a16_stream_t stream);
 
 /* Testing aid for failure detection: when `enable` is non-zero, the next
- * launch of the streaming kernel on any device skips issuing its weight
- * copies, so its waits for them run out (after about one second) and it
+ * launch of a CUDA-core GEMM kernel (decode GEMV or streaming) on any device
+ * skips issuing its weight copies, so its waits for them run out (after about one second) and it
  * records W4A16_ERR_TIMEOUT and returns. The switch clears itself after
  * that launch. No fault, trap or hang is involved; the context stays
  * usable. Not for production use. */

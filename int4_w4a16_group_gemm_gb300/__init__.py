@@ -11,6 +11,7 @@ Functions keep the C names:
     w4a16_quantize(w, group=32, stream=None) -> (qw, sc)
     w4a16_moe_sort(expert_ids, E, stream=None) -> (offsets, perm)
     w4a16_moe_workspace_size(T, topk, E, H, I) -> int
+    w4a16_moe_workspace_layout(T, topk, E, H, I) -> {"perm", "h", "o"} byte offsets
     w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn,
                    workspace=None, y=None, group=32, stream=None) -> y
     w4a16_moe_route(x, router_w, topk, bias=None, route_scale=1.0, stream=None)
@@ -41,7 +42,7 @@ W4A16_ERR_TIMEOUT = 5
 ACT_F32 = 0
 ACT_BF16 = 1
 
-ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+ALGOS = {"auto": 0, "simt": 1, "tc": 2, "stream": 3, "gemv": 4}
 FLAG_OVERLAP = 1
 FLAG_OUT_BF16 = 2
 
@@ -54,6 +55,8 @@ SIGNATURES = {
     "w4a16_quantize": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP]),
     "w4a16_moe_sort": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "w4a16_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "w4a16_moe_workspace_layout": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ),
+                                        ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "w4a16_moe_gemm": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
                             _VP, _SZ, _VP, _VP]),
     "w4a16_moe_gemm_noalloc": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _I, _I,
@@ -208,9 +211,17 @@ def w4a16_moe_workspace_size(T: int, topk: int, E: int, H: int, I: int) -> int:
     return int(lib.w4a16_moe_workspace_size(T, topk, E, H, I))
 
 
-def w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, workspace=None,
-                   y=None, group: int = 32, stream=None):
-    """Grouped MoE layer on INT4 experts -> y fp32 [T, H]."""
+def w4a16_moe_workspace_layout(T: int, topk: int, E: int, H: int, I: int) -> dict:
+    """Byte offsets of perm, h and o inside the MoE workspace (see the header)."""
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    code = lib.w4a16_moe_workspace_layout(T, topk, E, H, I, ctypes.byref(a), ctypes.byref(b),
+                                          ctypes.byref(c))
+    _check("w4a16_moe_workspace_layout", code)
+    return {"perm": a.value, "h": b.value, "o": c.value}
+
+
+def _moe_args(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y):
+    """Checks shared by the MoE layer wrappers -> (xdt, T, H, topk, E, I, y)."""
     import torch
     xdt = _act_dtype(x)
     _need(x, x.dtype, "x")
@@ -223,11 +234,22 @@ def w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, workspace
     topk = expert_ids.shape[1]
     E = qw_gu.shape[0]
     I = qw_gu.shape[1] // 2
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, "y")
+    if tuple(y.shape) != (T, H):
+        raise ValueError(f"y must have shape {(T, H)}, got {tuple(y.shape)}")
+    return xdt, T, H, topk, E, I, y
+
+
+def w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, workspace=None,
+                   y=None, group: int = 32, stream=None):
+    """Grouped MoE layer on INT4 experts -> y fp32 [T, H]."""
+    import torch
+    xdt, T, H, topk, E, I, y = _moe_args(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y)
     ws = w4a16_moe_workspace_size(T, topk, E, H, I)
     if workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=x.device)
-    if y is None:
-        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
     code = lib.w4a16_moe_gemm(_ptr(x), xdt, _ptr(expert_ids), _ptr(route_w), T, topk,
                               _ptr(qw_gu), _ptr(sc_gu), _ptr(qw_dn), _ptr(sc_dn), E, H, I, group,
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -239,18 +261,15 @@ def w4a16_moe_gemm(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, workspace
 def w4a16_moe_gemm_noalloc(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y=None,
                            group: int = 32, stream=None):
     """w4a16_moe_gemm without a workspace: the library's fixed 40 MiB device
-    array holds the intermediates (for callers that cannot allocate)."""
+    array holds the intermediates (for callers that cannot allocate). The
+    array used is the current device's, so every tensor must live there."""
     import torch
-    xdt = _act_dtype(x)
-    _need(x, x.dtype, "x")
-    _need(expert_ids, torch.int32, "expert_ids")
-    _need(route_w, torch.float32, "route_w")
-    T, H = x.shape
-    topk = expert_ids.shape[1]
-    E = qw_gu.shape[0]
-    I = qw_gu.shape[1] // 2
-    if y is None:
-        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    xdt, T, H, topk, E, I, y = _moe_args(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y)
+    cur = torch.cuda.current_device()
+    for t, n in ((x, "x"), (expert_ids, "expert_ids"), (route_w, "route_w"), (qw_gu, "qw_gu"),
+                 (sc_gu, "sc_gu"), (qw_dn, "qw_dn"), (sc_dn, "sc_dn"), (y, "y")):
+        if t.device.index != cur:
+            raise ValueError(f"{n} is on {t.device}, not on the current device cuda:{cur}")
     code = lib.w4a16_moe_gemm_noalloc(_ptr(x), xdt, _ptr(expert_ids), _ptr(route_w), T, topk,
                                       _ptr(qw_gu), _ptr(sc_gu), _ptr(qw_dn), _ptr(sc_dn), E, H, I,
                                       group, _ptr(y), _stream_handle(stream))
@@ -259,8 +278,9 @@ def w4a16_moe_gemm_noalloc(x, expert_ids, route_w, qw_gu, sc_gu, qw_dn, sc_dn, y
 
 
 def w4a16_debug_fault_next_launch(enable: bool = True) -> None:
-    """Testing aid: the next streaming-kernel launch skips its weight copies,
-    times out after about a second and records W4A16_ERR_TIMEOUT."""
+    """Testing aid: the next launch of a CUDA-core GEMM kernel (decode GEMV or
+    streaming) skips its weight copies, times out after about a second and
+    records W4A16_ERR_TIMEOUT."""
     lib.w4a16_debug_fault_next_launch(1 if enable else 0)
 
 

@@ -79,7 +79,7 @@ static inline w4a16_status from_cuda(cudaError_t e) {
 static constexpr int kTcMinM = 4;
 static constexpr int kTcF32MinM = 12;
 
-enum class GemmKernel { Stream, TensorBf16, TensorF32 };
+enum class GemmKernel { Stream, Gemv, TensorBf16, TensorF32 };
 
 // Kernel choice shared by the launch path and the launch-count query.
 // Returns OK and sets *kind, or the rejection status.
@@ -87,14 +87,19 @@ static w4a16_status plan_gemm(int M, int N, int K, int group, w4a16_act_dtype xd
                               w4a16_algo algo, GemmKernel *kind) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
   if (xdt != W4A16_ACT_F32 && xdt != W4A16_ACT_BF16) return W4A16_ERR_INVALID_ARG;
-  if (algo != W4A16_ALGO_AUTO && algo != W4A16_ALGO_SIMT && algo != W4A16_ALGO_TC)
+  if (algo != W4A16_ALGO_AUTO && algo != W4A16_ALGO_SIMT && algo != W4A16_ALGO_TC &&
+      algo != W4A16_ALGO_STREAM && algo != W4A16_ALGO_GEMV)
     return W4A16_ERR_INVALID_ARG;
   if (!group_supported(group)) return W4A16_ERR_UNSUPPORTED;
   if (K % group != 0) return W4A16_ERR_INVALID_ARG;
   const bool bf16 = xdt == W4A16_ACT_BF16;
   const bool f32_tc_ok = !bf16 && tc_f32_supported(M, N, K) && K <= max_k_stream(1);
+  const bool gemv_ok = gemv_supported(M, N, K, group);
   *kind = GemmKernel::Stream;
-  if (algo == W4A16_ALGO_TC) {
+  if (algo == W4A16_ALGO_GEMV) {
+    if (!gemv_ok) return W4A16_ERR_UNSUPPORTED;
+    *kind = GemmKernel::Gemv;
+  } else if (algo == W4A16_ALGO_TC) {
     if (bf16 && tc_gemm_supported(M, N, K))
       *kind = GemmKernel::TensorBf16;
     else if (f32_tc_ok)
@@ -139,6 +144,8 @@ w4a16_status w4a16_gemm_ex(const void *x, w4a16_act_dtype xdt, const int32_t *qw
   if (kind == GemmKernel::TensorBf16)
     return from_cuda(launch_tc_gemm(static_cast<const uint16_t *>(x), qw, sc, M, N, K, group, y,
                                     ybf16, overlap, s));
+  if (kind == GemmKernel::Gemv)
+    return from_cuda(launch_gemv(x, bf16, qw, sc, N, K, group, y, ybf16, overlap, s));
   if (kind == GemmKernel::TensorF32)
     return from_cuda(launch_tc_f32(static_cast<const float *>(x), qw, sc, M, N, K, group, y,
                                    ybf16, overlap, s));
@@ -176,6 +183,14 @@ w4a16_status w4a16_moe_sort(const int32_t *expert_ids, int n_pairs, int E, int32
 size_t w4a16_moe_workspace_size(int T, int topk, int E, int H, int I) {
   if (T < 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
   return moe_workspace_bytes(T, topk, E, H, I);
+}
+
+w4a16_status w4a16_moe_workspace_layout(int T, int topk, int E, int H, int I, size_t *off_perm,
+                                        size_t *off_h, size_t *off_o) {
+  if (T <= 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return W4A16_ERR_INVALID_ARG;
+  if (!off_perm || !off_h || !off_o) return W4A16_ERR_INVALID_ARG;
+  moe_workspace_offsets(T, topk, E, H, I, off_perm, off_h, off_o);
+  return W4A16_OK;
 }
 
 w4a16_status w4a16_moe_gemm(const void *x, w4a16_act_dtype xdt, const int32_t *expert_ids,

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/w4a16.h"
 
 namespace w4a16 {
@@ -19,6 +21,23 @@ struct DeviceInfo {
 
 // Per-device facts, looked up once per device (thread-safe).
 const DeviceInfo &device_info();
+
+// One-time set-up per device (function attributes such as the dynamic
+// shared-memory opt-in are per device): run() calls `fn` once for the
+// current device and returns its result on every later call there.
+struct PerDeviceOnce {
+  static constexpr int kDevices = 64;
+  std::once_flag flag[kDevices];
+  cudaError_t err[kDevices] = {};
+  template <class F>
+  cudaError_t run(F &&fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices)
+      return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { err[dev] = fn(); });
+    return err[dev];
+  }
+};
 
 // Testing aid: true once after w4a16_debug_fault_next_launch(1); the
 // streaming kernel launched then skips its weight copies.
@@ -41,6 +60,16 @@ int stream_tile(int M, int K);
 // Number of streaming-kernel launches for M tokens (1 unless the tiles
 // exceed the grid's y limit).
 int stream_gemm_passes(int M, int K);
+
+// ------------------------------------------------------------ decode GEMV kernel
+// y = x * W_hat^T for one token (M = 1) on CUDA cores, one CTA per SM sized
+// so that the next call's CTA can prefetch its weights beside it (see
+// gemv.cu). Same `y_bf16` and `overlap` contract as the streaming kernel.
+constexpr int kGemvMaxK = 8192;
+bool gemv_supported(int M, int N, int K, int group);
+cudaError_t launch_gemv(const void *x, bool x_bf16, const int32_t *qw, const float *sc, int N,
+                        int K, int group, void *y, bool y_bf16, bool overlap,
+                        cudaStream_t stream);
 
 // ------------------------------------------------------------ tensor-core kernel
 // Same contract for bf16 activations on tcgen05 tensor cores, including
@@ -70,6 +99,10 @@ cudaError_t launch_quantize(const float *w, int N, int K, int group, int32_t *qw
 cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *offsets,
                             int32_t *perm, cudaStream_t stream);
 size_t moe_workspace_bytes(int T, int topk, int E, int H, int I);
+// Byte offsets inside that workspace of the expert-sorted pair order, the
+// SwiGLU outputs h and the per-slot outputs o.
+void moe_workspace_offsets(int T, int topk, int E, int H, int I, size_t *off_perm, size_t *off_h,
+                           size_t *off_o);
 // `shared_o` ([T][H] fp32, or nullptr) is added to every token's output
 // after its routed slots (the shared expert's output).
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,

@@ -451,11 +451,10 @@ cudaError_t launch_expert_kernel(MoeParams p, int K, int L, int max_items, const
   p.nstages = ns;
   const size_t smem = bytes_for(ns);
   auto kern = moe_expert_kernel<MT, WPL, BF16, MODE, MAXW, MINB>;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(budget));
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr_err = attr_once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(budget));
   });
   if (attr_err != cudaSuccess) return attr_err;
   kern<<<dim3(max_items, gx), threads, smem, stream>>>(p);
@@ -488,6 +487,14 @@ cudaError_t launch_moe_sort(const int32_t *ids, int n_pairs, int E, int32_t *off
 
 size_t moe_workspace_bytes(int T, int topk, int E, int H, int I) {
   return ws_layout(T, topk, E, H, I).total;
+}
+
+void moe_workspace_offsets(int T, int topk, int E, int H, int I, size_t *off_perm, size_t *off_h,
+                           size_t *off_o) {
+  const WsLayout L = ws_layout(T, topk, E, H, I);
+  *off_perm = L.off_perm;
+  *off_h = L.off_h;
+  *off_o = L.off_o;
 }
 
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,

@@ -289,11 +289,10 @@ cudaError_t launch_tiles(const StreamParams &base, int tiles, int N, int K, int 
   p.nstages = ns;
   const size_t smem = bytes_for(ns);
   auto kern = stream_gemm_kernel<MT, WPL, BF16, SCB, MAXW, MINB>;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_optin - 1024);
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr_err = attr_once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_optin - 1024);
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchAttribute attr[1];

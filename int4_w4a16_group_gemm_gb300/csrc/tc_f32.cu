@@ -481,11 +481,9 @@ cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, in
   const int ks = std::max(1, std::min(std::min(env_ks > 0 ? std::min(env_ks, 4) : 4, nk),
                                       di.num_sms / std::max(1, p.num_tiles)));
   auto kern = tc_f32_kernel;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FX_SMEM);
-  });
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr_err = attr_once.run(
+      [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FX_SMEM); });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_tiles, ks);

@@ -370,10 +370,9 @@ cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, bo
                       cudaStream_t stream) {
   using Cfg = TcCfg<BM, SUBS>;
   auto kern = tc_gemm_kernel<BM, SUBS>;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr_err = attr_once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};

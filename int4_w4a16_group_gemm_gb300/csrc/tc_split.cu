@@ -382,11 +382,9 @@ cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *s
     ks *= 2;
 
   auto kern = tc_split_kernel;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM);
-  });
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr_err = attr_once.run(
+      [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM); });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_tiles, ks);

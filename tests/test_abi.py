@@ -152,6 +152,17 @@ def test_binding_rejects_host_tensors(w4):
         w4.w4a16_quantize(torch.zeros((8, 64), dtype=torch.float32))
     with pytest.raises(TypeError):
         w4.w4a16_gemm(x.double(), qw, sc)  # neither fp32 nor bf16
+    # the MoE layer wrappers check every tensor, the weights and y included
+    xm = torch.zeros((2, 64), dtype=torch.float32)
+    ids = torch.zeros((2, 1), dtype=torch.int32)
+    rw = torch.ones((2, 1), dtype=torch.float32)
+    qgu = torch.zeros((1, 64, 8), dtype=torch.int32)
+    sgu = torch.zeros((1, 64, 2), dtype=torch.float32)
+    qdn = torch.zeros((1, 64, 4), dtype=torch.int32)
+    sdn = torch.zeros((1, 64, 1), dtype=torch.float32)
+    for fn in (w4.w4a16_moe_gemm, w4.w4a16_moe_gemm_noalloc):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            fn(xm, ids, rw, qgu, sgu, qdn, sdn)
 
 
 def test_package_without_library_fails_to_import(tmp_path):

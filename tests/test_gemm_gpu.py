@@ -451,3 +451,74 @@ def test_graph_replay_with_overlap_matches_oracle(w4, M, N, K, dt):
             err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
             assert np.all(err <= TOL[dt] * bound), f"copy {c}: max err/bound {np.max(err / bound):.3e}"
         assert torch.equal(ys[c].view(torch.int32), ys[c + ncopies].view(torch.int32))
+
+
+# The decode GEMV kernel (one token, one CTA per SM, weights prefetched
+# across calls) and the streaming kernel at M = 1, each forced, against the
+# oracle: the decode shape, ragged N (fewer rows than SMs, rows not a
+# multiple of the 4-row stage), one-word-only warps (small K), all-two-word
+# warps (K = 8192), more stages than ring slots (refills), group 128.
+GEMV_CASES = [
+    # N, K, group
+    (4096, 7168, 32), (1, 128, 32), (7, 2048, 32), (153, 8192, 32), (5000, 4096, 32),
+    (9728, 7168, 32), (4096, 7168, 128), (300, 1024, 64), (2, 256, 64),
+]
+
+
+@pytest.mark.parametrize("algo", ["gemv", "stream"])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("N,K,group", GEMV_CASES)
+def test_decode_kernels_m1(w4, algo, dt, N, K, group):
+    _, ratio = run_case(w4, 1, N, K, dt, seed=N + K + group, algo=algo, group=group)
+    if dt == "f32":
+        assert ratio < 0.1
+
+
+def test_gemv_kernel_rejects_other_shapes(w4):
+    # M = 1 with K <= 8192 and whole 16-byte scale rows: one launch of it
+    assert w4.w4a16_gemm_launches(1, 4096, 7168, "f32", "gemv") == 1
+    for M, N, K in ((2, 64, 256), (1, 64, 8448), (1, 64, 96)):
+        x = torch.zeros((M, K), dtype=torch.float32, device="cuda")
+        qw = torch.zeros((N, K // 8), dtype=torch.int32, device="cuda")
+        sc = torch.zeros((N, K // 32), dtype=torch.float32, device="cuda")
+        with pytest.raises(w4.W4A16Error) as ei:
+            w4.w4a16_gemm(x, qw, sc, algo="gemv")
+        assert ei.value.code == w4.W4A16_ERR_UNSUPPORTED
+    # the same call twice: identical bits (fixed reduction order)
+    x = torch.from_numpy(synth.activations(50, 1, 7168)).cuda()
+    qw, sc = w4.w4a16_quantize(torch.from_numpy(synth.weights(50, 4096, 7168)).cuda())
+    a = w4.w4a16_gemm(x, qw, sc, algo="gemv")
+    b = w4.w4a16_gemm(x, qw, sc, algo="gemv")
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_gemv_overlap_chain_long(w4, dt):
+    """Twelve overlapped decode GEMVs, each consuming the previous output,
+    into NaN-poisoned buffers (so the next call's CTAs prefetch beside the
+    running call for the whole chain): same bits as the plain chain."""
+    K, n = 4096, 12
+    x = synth.activations(51, 1, K)
+    dev = [w4.w4a16_quantize(torch.from_numpy(synth.weights(51, K, K, sub=i)).cuda())
+           for i in range(n)]
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+
+    def chain(overlap):
+        outs = [torch.full((1, K), float("nan"), device="cuda") for _ in dev]
+        ins = [torch.full((1, K), float("nan"), device="cuda", dtype=dtype) for _ in dev]
+        torch.cuda.synchronize()
+        ins[0].copy_(torch.from_numpy(x).to(dtype))
+        for i, (qw, sc) in enumerate(dev):
+            # scale down so that the chain stays in range
+            w4.w4a16_gemm(ins[i], qw, sc, y=outs[i], algo="gemv", overlap=overlap)
+            if i + 1 < n:
+                ins[i + 1].copy_((outs[i] * 0.5).to(dtype))
+        torch.cuda.synchronize()
+        return outs
+
+    plain = chain(False)
+    over = chain(True)
+    assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    for a, b in zip(plain, over):
+        assert torch.isfinite(a).all()
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
