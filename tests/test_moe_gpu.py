@@ -7,7 +7,15 @@
   SwiGLU, the bf16 rounding of h and the slot sum);
 * the full-size layer (128 tokens, hidden 7168, 384 experts of 2048-wide
   SwiGLU, top-8) is checked on sampled tokens: the oracle rebuilds the
-  experts those tokens use from the same seeded draws.
+  experts those tokens use from the same seeded draws;
+* stage by stage (the device leaves its intermediates in the workspace,
+  w4a16_moe_workspace_layout says where): the expert-sorted pair order is
+  bit-exact; each SwiGLU output h is within the gate/up GEMM bound
+  propagated through SwiGLU (plus the bf16 rounding of h in bf16 mode);
+  each per-slot output o is within the down GEMM's own bound when the
+  oracle's down GEMM is fed the device's h; y is the slot-ordered fp32 sum
+  of the device's o. At full size the stage checks cover every token of
+  experts chosen to have 1, 2, 3 and more than 3 tokens.
 """
 
 import numpy as np
@@ -64,19 +72,74 @@ def build_experts_host(seed, E, H, I, group=32):
     return np.stack(qgu), np.stack(sgu), np.stack(qdn), np.stack(sdn)
 
 
+def read_stages(w4, ws, T, topk, E, H, I, bf16):
+    """The device's intermediates from the workspace: perm [n], h [n, I]
+    (by sorted position, as float64) and o [n, H] (by pair)."""
+    L = w4.w4a16_moe_workspace_layout(T, topk, E, H, I)
+    n = T * topk
+    raw = ws.cpu()
+    perm = raw[L["perm"]:L["perm"] + 4 * n].view(torch.int32).numpy().copy()
+    hb = raw[L["h"]:L["h"] + (2 if bf16 else 4) * n * I]
+    h = (hb.view(torch.bfloat16).float() if bf16 else hb.view(torch.float32)).numpy()
+    o = raw[L["o"]:L["o"] + 4 * n * H].view(torch.float32).numpy()
+    return perm, h.reshape(n, I).astype(np.float64), o.reshape(n, H).astype(np.float64)
+
+
+def check_stages(x, ids, rw, experts, perm, h, o, y, bf16, eps, group=32, only=None):
+    """Stage-wise parity. `experts[e]` = (qw_gu, sc_gu, qw_dn, sc_dn) host
+    arrays; `only` restricts the h and o checks to those experts."""
+    T, topk = ids.shape
+    _, ro = oracle.moe_sort(ids, max(int(ids.max()) + 1, 1))
+    np.testing.assert_array_equal(perm, ro)
+    pos = {int(p): s for s, p in enumerate(perm)}
+    by_expert = {}
+    for p in range(T * topk):
+        by_expert.setdefault(int(ids.reshape(-1)[p]), []).append(p)
+    checked = 0
+    for e, pairs in sorted(by_expert.items()):
+        if only is not None and e not in only:
+            continue
+        qgu, sgu, qdn, sdn = experts[e]
+        toks = [p // topk for p in pairs]
+        hr, ht = oracle.moe_swiglu_ref(x[toks], qgu, sgu, bf16, eps, group)
+        hd = h[[pos[p] for p in pairs]]
+        err = np.abs(hd - hr)
+        assert np.all(err <= ht), f"expert {e} h: max err/tol {np.max(err / ht):.3e}"
+        rws = rw.reshape(-1)[pairs]
+        orf, ot = oracle.moe_down_ref(hd, rws, qdn, sdn, eps, group)
+        err = np.abs(o[pairs] - orf)
+        assert np.all(err <= ot), f"expert {e} o: max err/tol {np.max(err / ot):.3e}"
+        checked += len(pairs)
+    # combine: y[t] is the fp32 sum of the token's slots in slot order
+    os_ = o.reshape(T, topk, -1)
+    ysum = os_.sum(axis=1)
+    bound = topk * 2.0 ** -24 * np.abs(os_).sum(axis=1)
+    assert np.all(np.abs(y - ysum) <= bound)
+    return checked
+
+
 def check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16, group=32):
     xt = torch.from_numpy(x)
     if bf16:
         xt = xt.to(torch.bfloat16)
     dev = [torch.from_numpy(a).cuda() for a in (qgu, sgu, qdn, sdn)]
+    T, H = x.shape
+    topk, E, I = ids.shape[1], qgu.shape[0], qgu.shape[1] // 2
+    ws = torch.empty(w4.w4a16_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8,
+                     device="cuda")
     y = w4.w4a16_moe_gemm(xt.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(rw).cuda(),
-                          *dev, group=group)
+                          *dev, workspace=ws, group=group)
     torch.cuda.synchronize()
     assert w4.w4a16_last_device_status() == w4.W4A16_OK
-    ref, tol = oracle.moe_ref(xt.float().numpy(), ids, rw, qgu, sgu, qdn, sdn, bf16,
-                              eps=4e-3 if bf16 else 1e-5, group=group)
-    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    eps = 4e-3 if bf16 else 1e-5
+    xo = xt.float().numpy()
+    ref, tol = oracle.moe_ref(xo, ids, rw, qgu, sgu, qdn, sdn, bf16, eps=eps, group=group)
+    yh = y.cpu().numpy().astype(np.float64)
+    err = np.abs(yh - ref)
     assert np.all(err <= tol), f"max err/tol = {np.max(err / tol):.3e}"
+    perm, h, o = read_stages(w4, ws, T, topk, E, H, I, bf16)
+    experts = {e: (qgu[e], sgu[e], qdn[e], sdn[e]) for e in range(E)}
+    check_stages(xo, ids, rw, experts, perm, h, o, yh, bf16, eps, group)
     return y
 
 
@@ -139,12 +202,24 @@ def test_full_size_moe_sampled_tokens(w4):
         w4.w4a16_quantize(synth.weights_device(seed, 2 * I, H, dev, sub=2 * e), qw=qgu[e], sc=sgu[e])
         w4.w4a16_quantize(synth.weights_device(seed, H, I, dev, sub=2 * e + 1), qw=qdn[e], sc=sdn[e])
     xb = torch.from_numpy(x).to(torch.bfloat16)
+    ws = torch.empty(w4.w4a16_moe_workspace_size(T, topk, E, H, I), dtype=torch.uint8, device=dev)
     y = w4.w4a16_moe_gemm(xb.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(rw).cuda(),
-                          qgu, sgu, qdn, sdn)
+                          qgu, sgu, qdn, sdn, workspace=ws)
     torch.cuda.synchronize()
     assert w4.w4a16_last_device_status() == w4.W4A16_OK
+    yh = y.cpu().numpy().astype(np.float64)
+    xo = xb.float().numpy()
+
+    # experts with 1, 2, 3 and the most tokens (two of each), plus the
+    # experts of two sampled tokens for the end-to-end check
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    chosen = []
+    for c in (1, 2, 3):
+        chosen += [int(e) for e in np.flatnonzero(counts == c)[:2]]
+    chosen += [int(e) for e in np.argsort(-counts, kind="stable")[:2]]
+    assert counts[chosen[-1]] > 3
     tokens = [0, 77]
-    used = sorted({int(e) for t in tokens for e in ids[t]})
+    used = sorted(set(chosen) | {int(e) for t in tokens for e in ids[t]})
     hq = {}
     for e in used:
         wg = synth.weights_device(seed, 2 * I, H, dev, sub=2 * e).cpu().numpy()
@@ -154,11 +229,16 @@ def test_full_size_moe_sampled_tokens(w4):
         # the device packing the GPU used is the oracle's packing
         assert np.array_equal(a, qgu[e].cpu().numpy()) and np.array_equal(c, qdn[e].cpu().numpy())
         hq[e] = (a, b, c, d)
-    ref, tol = oracle.moe_ref(xb.float().numpy(), ids, rw,
+
+    perm, h, o = read_stages(w4, ws, T, topk, E, H, I, True)
+    checked = check_stages(xo, ids, rw, hq, perm, h, o, yh, True, 4e-3, only=set(chosen))
+    covered = {p // topk for p in range(T * topk) if int(ids.reshape(-1)[p]) in chosen}
+    assert checked >= 16 and len(covered) >= 16
+
+    ref, tol = oracle.moe_ref(xo, ids, rw,
                               {e: v[0] for e, v in hq.items()}, {e: v[1] for e, v in hq.items()},
                               {e: v[2] for e, v in hq.items()}, {e: v[3] for e, v in hq.items()},
                               True, eps=4e-3, tokens=tokens)
-    yh = y.cpu().numpy().astype(np.float64)
     for t in tokens:
         err = np.abs(yh[t] - ref[t])
         assert np.all(err <= tol[t]), f"token {t}: max err/tol = {np.max(err / tol[t]):.3e}"

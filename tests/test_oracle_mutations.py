@@ -4,8 +4,8 @@ Each case plants one mistake in the oracle (on the CPU, by replacing one
 oracle function for the duration of the test) and checks that a pin of
 tests/test_oracle_pins.py then fails: a wrong nibble order, a dropped zero
 point, the wrong rounding mode or scale in the quantiser, a wrong group
-index, a swapped gate/up or a wrong activation in SwiGLU, ties broken the
-other way or unnormalised weights in the router, a mis-weighted shared
+index, a swapped gate/up or a wrong activation in SwiGLU (in the layer and in
+its SwiGLU stage), a transposed down-stage weight, ties broken the other way or unnormalised weights in the router, a mis-weighted shared
 expert.
 """
 
@@ -130,3 +130,29 @@ def test_misweighted_shared_expert_is_caught(monkeypatch):
         return real(x, ids, rw, *a, **k)
     monkeypatch.setattr(oracle, "moe_ref", moe_ref_half_last_slot)
     fails(pins.test_moe_block_shared_expert_closed_forms)
+
+
+def test_down_stage_transposed_weight_is_caught(monkeypatch):
+    real_deq = oracle.dequantize
+
+    def down_transposed(h_in, route_w, qw_dn, sc_dn, eps, group=32):
+        h_in = np.asarray(h_in, dtype=np.float64)
+        r = np.asarray(route_w, dtype=np.float32).astype(np.float64)
+        w = real_deq(qw_dn, sc_dn, group).astype(np.float64)
+        o = r[:, None] * (h_in @ w)          # W instead of W^T
+        return o, np.abs(o)
+    monkeypatch.setattr(oracle, "moe_down_ref", down_transposed)
+    fails(pins.test_moe_down_stage_matches_brute_force_and_scales)
+
+
+def test_swiglu_stage_gate_up_swapped_is_caught(monkeypatch):
+    real_deq = oracle.dequantize
+
+    def swiglu_swapped(x, qw_gu, sc_gu, bf16_mode, eps, group=32):
+        w = real_deq(qw_gu, sc_gu, group).astype(np.float64)
+        I = w.shape[0] // 2
+        gu = np.asarray(x, dtype=np.float64) @ w.T
+        h = oracle.silu(gu[:, I:]) * gu[:, :I]   # silu(up) * gate
+        return h, np.abs(h) + 1.0
+    monkeypatch.setattr(oracle, "moe_swiglu_ref", swiglu_swapped)
+    fails(pins.test_moe_swiglu_stage_matches_brute_force)

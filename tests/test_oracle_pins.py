@@ -493,6 +493,58 @@ def test_moe_ref_token_permutation_and_slot_order():
     assert not sub[[0, 2, 4]].any()
 
 
+def test_moe_swiglu_stage_matches_brute_force():
+    """One expert's gate/up GEMM and SwiGLU against a pure-Python loop (exact
+    sums with math.fsum), in both modes; the bf16-mode tolerance covers the
+    rounding of h to bf16."""
+    pytest.importorskip("torch")
+    x, ids, rw, qgu, sgu, qdn, sdn = _tiny_moe(31, T=3, E=2)
+    for bf16_mode in (False, True):
+        xs = oracle.round_to_bf16(x) if bf16_mode else x
+        h, tol = oracle.moe_swiglu_ref(xs, qgu[1], sgu[1], bf16_mode, eps=4e-3)
+        wgu = brute_dequant(qgu[1], sgu[1])
+        I = len(wgu) // 2
+        for m in range(xs.shape[0]):
+            gu = [math.fsum(float(xs[m, k]) * wgu[r][k] for k in range(xs.shape[1]))
+                  for r in range(2 * I)]
+            hb = [gu[i] / (1.0 + math.exp(-gu[i])) * gu[I + i] for i in range(I)]
+            np.testing.assert_allclose(h[m], hb, rtol=1e-12, atol=1e-15)
+        assert (tol > 0).all()
+        if bf16_mode:  # the device stores h rounded to bf16
+            hb16 = oracle.round_to_bf16(h.astype(np.float32)).astype(np.float64)
+            assert np.all(np.abs(hb16 - h) <= tol)
+
+
+def test_moe_down_stage_matches_brute_force_and_scales():
+    """One expert's down GEMM fed a given h, times the routing weight, against
+    a pure-Python loop; doubling the weight doubles the output exactly."""
+    x, ids, rw, qgu, sgu, qdn, sdn = _tiny_moe(32, T=3, E=2)
+    h = synth.activations(33, 3, 32).astype(np.float64)
+    r = np.array([0.25, -1.5, 3.0], np.float32)
+    o, tol = oracle.moe_down_ref(h, r, qdn[0], sdn[0], eps=4e-3)
+    wdn = brute_dequant(qdn[0], sdn[0])
+    for m in range(3):
+        for n in range(len(wdn)):
+            ob = float(r[m]) * math.fsum(h[m, i] * wdn[n][i] for i in range(h.shape[1]))
+            assert o[m, n] == pytest.approx(ob, rel=1e-12, abs=1e-15)
+    o2, tol2 = oracle.moe_down_ref(h, 2 * r, qdn[0], sdn[0], eps=4e-3)
+    np.testing.assert_array_equal(o2, 2 * o)
+    np.testing.assert_array_equal(tol2, 2 * tol)
+    assert np.all(tol >= 4e-3 * np.abs(o))  # sum|h*w| bounds |sum h*w|
+
+
+def test_moe_stages_compose_to_the_layer():
+    """Top-1 routing in fp32 mode: the layer is the down stage fed the SwiGLU
+    stage's h, with the routing weight."""
+    x, ids, rw, qgu, sgu, qdn, sdn = _tiny_moe(34, T=4, E=3, topk=1)
+    y, _ = oracle.moe_ref(x, ids, rw, qgu, sgu, qdn, sdn, False, eps=1e-5)
+    for t in range(4):
+        e = int(ids[t, 0])
+        h, _ = oracle.moe_swiglu_ref(x[t:t + 1], qgu[e], sgu[e], False, eps=1e-5)
+        o, _ = oracle.moe_down_ref(h, rw[t:t + 1, 0], qdn[e], sdn[e], eps=1e-5)
+        np.testing.assert_allclose(y[t], o[0], rtol=1e-13, atol=1e-15)
+
+
 # ------------------------------------------------------------ MoE routing and block
 def brute_route(x, wr, bias, topk, scale):
     """Pure-Python routing: exact rational logits, math.exp sigmoid, sort by key."""
