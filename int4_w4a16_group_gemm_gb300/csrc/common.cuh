@@ -209,6 +209,90 @@ __device__ __forceinline__ uint64_t nibble_pair(uint32_t word, uint32_t word_sh8
 // Pre-scale factor of the activation matching a class-c nibble.
 __host__ __device__ constexpr float nibble_prescale(int c) { return (c & 1) ? 0.0625f : 1.0f; }
 
+// ---------------------------------------------------------------- fp32 pairs
+// Packed fp32 pairs: Blackwell's add/fma.f32x2 do two independent fp32
+// operations (each rounded exactly like the scalar one) per instruction.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------- unpack
+// Exact fp32 (nibble - 8) of the same nibble position of two packed words,
+// as the two halves of one packed fp32 pair, with one logic instruction per
+// value and one packed subtract per pair:
+//   nibble j of a word sits in bits 4j..4j+3. For j <= 4 those bits lie in
+//   the fp32 mantissa; ORing them into the bits of 2^(23-4j) (mantissa 0)
+//   gives the fp32 number 2^(23-4j) + nibble exactly (the mantissa's unit
+//   in the last place is 2^(-4j) there, times 2^(4j) for the nibble's
+//   position). Subtracting 2^(23-4j) + 8 leaves nibble - 8, exact.
+//   Nibbles 5..7 are taken from the word shifted right by 12, where they sit
+//   at positions 2..4.
+// The GPU's logic pipe runs at half the rate of its fp32 pipe, so the
+// unpack is written as explicit lop3 ((w & mask) | magic in one
+// instruction; the compiler otherwise emits an AND and an OR) and packed
+// fp32 arithmetic; values never pass through fp16 halves, whose extraction
+// costs further logic instructions.
+struct PairUnpack {
+  uint32_t magic[5];  // fp32 bits of 2^(23-4j)
+};
+
+__device__ __forceinline__ PairUnpack make_pair_unpack() {
+  PairUnpack k;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) k.magic[j] = opaque_u32(static_cast<uint32_t>(127 + 23 - 4 * j) << 23);
+  return k;
+}
+
+// The packed bias -(2^(23-4j) + 8) of nibble position j (a compile-time
+// constant, which the compiler may keep outside the register file).
+template <int J>
+__device__ __forceinline__ uint64_t pair_bias() {
+  constexpr float b = -static_cast<float>((1u << (23 - 4 * J)) + 8u);
+  return (static_cast<uint64_t>(__float_as_uint(b)) << 32) | __float_as_uint(b);
+}
+
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t o) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(o));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pair_u32(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+// v[j] = (nibble j of a - 8, nibble j of b - 8), j = 0..7.
+__device__ __forceinline__ void unpack8_pair(uint32_t a, uint32_t b, const PairUnpack &k,
+                                             uint64_t (&v)[8]) {
+  const uint32_t a12 = a >> 12, b12 = b >> 12;
+  v[0] = add_f32x2(pair_u32(lop_and_or<0xFu>(a, k.magic[0]), lop_and_or<0xFu>(b, k.magic[0])), pair_bias<0>());
+  v[1] = add_f32x2(pair_u32(lop_and_or<0xF0u>(a, k.magic[1]), lop_and_or<0xF0u>(b, k.magic[1])), pair_bias<1>());
+  v[2] = add_f32x2(pair_u32(lop_and_or<0xF00u>(a, k.magic[2]), lop_and_or<0xF00u>(b, k.magic[2])), pair_bias<2>());
+  v[3] = add_f32x2(pair_u32(lop_and_or<0xF000u>(a, k.magic[3]), lop_and_or<0xF000u>(b, k.magic[3])), pair_bias<3>());
+  v[4] = add_f32x2(pair_u32(lop_and_or<0xF0000u>(a, k.magic[4]), lop_and_or<0xF0000u>(b, k.magic[4])), pair_bias<4>());
+  v[5] = add_f32x2(pair_u32(lop_and_or<0xF00u>(a12, k.magic[2]), lop_and_or<0xF00u>(b12, k.magic[2])), pair_bias<2>());
+  v[6] = add_f32x2(pair_u32(lop_and_or<0xF000u>(a12, k.magic[3]), lop_and_or<0xF000u>(b12, k.magic[3])), pair_bias<3>());
+  v[7] = add_f32x2(pair_u32(lop_and_or<0xF0000u>(a12, k.magic[4]), lop_and_or<0xF0000u>(b12, k.magic[4])), pair_bias<4>());
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }

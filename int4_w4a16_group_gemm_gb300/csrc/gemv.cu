@@ -70,65 +70,6 @@ struct GemvParams {
   int *status;
 };
 
-// ---------------------------------------------------------------- unpack
-// Exact fp32 (nibble - 8) of the same nibble position of two packed words,
-// as the two halves of one packed fp32 pair, with one logic instruction per
-// value and one packed subtract per pair:
-//   nibble j of a word sits in bits 4j..4j+3. For j <= 4 those bits lie in
-//   the fp32 mantissa; ORing them into the bits of 2^(23-4j) (mantissa 0)
-//   gives the fp32 number 2^(23-4j) + nibble exactly (the mantissa's unit
-//   in the last place is 2^(-4j) there, times 2^(4j) for the nibble's
-//   position). Subtracting 2^(23-4j) + 8 leaves nibble - 8, exact.
-//   Nibbles 5..7 are taken from the word shifted right by 12, where they sit
-//   at positions 2..4.
-// The GPU's logic pipe runs at half the rate of its fp32 pipe, so the
-// unpack is written as explicit lop3 ((w & mask) | magic in one
-// instruction; the compiler otherwise emits an AND and an OR) and packed
-// fp32 arithmetic; values never pass through fp16 halves, whose extraction
-// costs further logic instructions.
-struct PairUnpack {
-  uint32_t magic[5];  // fp32 bits of 2^(23-4j)
-  uint64_t bias[5];   // packed -(2^(23-4j) + 8)
-};
-
-__device__ __forceinline__ PairUnpack make_pair_unpack() {
-  PairUnpack k;
-#pragma unroll
-  for (int j = 0; j < 5; ++j) {
-    k.magic[j] = opaque_u32(static_cast<uint32_t>(127 + 23 - 4 * j) << 23);
-    const float b = opaque_f32(-static_cast<float>((1u << (23 - 4 * j)) + 8u));
-    k.bias[j] = pack_f32x2(b, b);
-  }
-  return k;
-}
-
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t o) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(o));
-  return d;
-}
-
-__device__ __forceinline__ uint64_t pair_u32(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-
-// v[j] = (nibble j of a - 8, nibble j of b - 8), j = 0..7.
-__device__ __forceinline__ void unpack8_pair(uint32_t a, uint32_t b, const PairUnpack &k,
-                                             uint64_t (&v)[8]) {
-  const uint32_t a12 = a >> 12, b12 = b >> 12;
-  v[0] = add_f32x2(pair_u32(lop_and_or<0xFu>(a, k.magic[0]), lop_and_or<0xFu>(b, k.magic[0])), k.bias[0]);
-  v[1] = add_f32x2(pair_u32(lop_and_or<0xF0u>(a, k.magic[1]), lop_and_or<0xF0u>(b, k.magic[1])), k.bias[1]);
-  v[2] = add_f32x2(pair_u32(lop_and_or<0xF00u>(a, k.magic[2]), lop_and_or<0xF00u>(b, k.magic[2])), k.bias[2]);
-  v[3] = add_f32x2(pair_u32(lop_and_or<0xF000u>(a, k.magic[3]), lop_and_or<0xF000u>(b, k.magic[3])), k.bias[3]);
-  v[4] = add_f32x2(pair_u32(lop_and_or<0xF0000u>(a, k.magic[4]), lop_and_or<0xF0000u>(b, k.magic[4])), k.bias[4]);
-  v[5] = add_f32x2(pair_u32(lop_and_or<0xF00u>(a12, k.magic[2]), lop_and_or<0xF00u>(b12, k.magic[2])), k.bias[2]);
-  v[6] = add_f32x2(pair_u32(lop_and_or<0xF000u>(a12, k.magic[3]), lop_and_or<0xF000u>(b12, k.magic[3])), k.bias[3]);
-  v[7] = add_f32x2(pair_u32(lop_and_or<0xF0000u>(a12, k.magic[4]), lop_and_or<0xF0000u>(b12, k.magic[4])), k.bias[4]);
-}
-
 // Activations of one word (8 columns from k0), fp32 or bf16 -> fp32 x[8].
 template <bool BF16>
 __device__ __forceinline__ void load_x8(const void *x, int k0, bool active, float (&xv)[8]) {

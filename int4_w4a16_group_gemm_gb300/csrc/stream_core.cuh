@@ -27,27 +27,6 @@ constexpr int kRowsPerChunk = 8;
 // lane's activations).
 __host__ __device__ constexpr int stream_max_threads(int, int = 0) { return 512; }
 
-// Packed fp32 pairs: Blackwell's add/fma.f32x2 do two independent fp32
-// operations (each rounded exactly like the scalar one) per instruction.
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
 // Load this lane's EPL activations of token row `xrow` (nullptr -> zeros),
 // pre-scaled by the nibble-class factor of each column, as pairs: pair
 // 4*i + c of word i holds columns 8i + c and 8i + 4 + c (the two nibbles of
