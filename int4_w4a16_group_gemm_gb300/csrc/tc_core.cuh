@@ -44,10 +44,6 @@ __device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t 
       : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -164,51 +160,146 @@ __device__ __forceinline__ void tc_mma_tmem_a(uint32_t dtmem, uint32_t atmem, ui
       : "memory");
 }
 
-// Load 16 bytes from the shared memory of cluster rank `rank` at the
-// address of `p` in this CTA (p 16-byte aligned).
-__device__ __forceinline__ float4 ld_cluster_f32x4(const float *p, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
+// Warp-wide forms of MMA issue and commit: every lane of a converged warp
+// executes them with the same operands and one elected lane issues. Run
+// from a single-lane branch, each MMA first moves its operands into uniform
+// registers, which makes issue slower than the tensor core at N = 64 and
+// several times slower again while other warps compete for issue slots; a
+// warp-uniform issuing loop keeps the operands uniform.
+__device__ __forceinline__ void tc_mma_tmem_a_warp(uint32_t dtmem, uint32_t atmem, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtmem),
+      "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_warp(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
 }
 
-// Split-K reduction by the owner of a row slice. Every CTA of the cluster
-// has parked its fp32 partial tile at red[row * LD + column] (BM columns) in
-// its shared memory and passed a cluster barrier. This CTA owns rows
-// lo .. lo + my_rows - 1: it reads 4 columns of a row from every rank
-// (16-byte distributed shared-memory loads, all issued before the sums),
-// adds them in rank order and stores y[m0 + m][n0 + row] for m0 + m < M and
+// ------------------------------------------------ split-K reduction by push
+// A tile of ROWS weight rows x BM tokens is split over K across the ks CTAs
+// (ranks) of a cluster; rank r owns the row slice [r R, (r + 1) R), R = ROWS / ks.
+// Every rank parks its fp32 partial tile at red[row * LD + column] in its
+// own shared memory and sends each other rank that rank's slice with one
+// bulk shared -> shared copy (the copy engine moves it; completion is
+// counted in bytes on the owner's mbarrier). The owner adds the ks partials
+// of its slice in rank order, so the result does not depend on timing.
+// Received slices go to a dedicated buffer (slot k < r for sender k < r,
+// k - 1 otherwise), never to memory the owner may still be using.
+//
+// Protocol (all waits bounded):
+//   set-up   one thread: mbar_init(bar, 1); push_expect(bar, ks); the
+//            barrier inits are fenced (fence_mbar_init) and then every
+//            thread does cluster_arrive() (phase A);
+//   end      every thread: cluster_wait() (phase A: every rank's barrier
+//            is initialised), then one thread push_send(); every thread
+//            waits for `bar`, cluster_arrive() (phase B: this rank has
+//            received), push_owner_sum(), cluster_wait() (phase B: every
+//            copy this CTA sent has landed, so its shared memory may go).
+// Relaxed arrive: neither phase publishes ordinary stores (the barrier
+// inits are published by fence_mbar_init, the slices by the copy engine's
+// byte count), and a release here waits for every outstanding store of the
+// thread.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of this CTA's shared-memory word `saddr` in the CTA of cluster
+// rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));
+  return a;
+}
+
+// ks is a power of two (1 .. MAXKS) that divides ROWS: slices are equal,
+// ROWS >> log2(ks) rows each, and no division is needed.
+__device__ __forceinline__ int log2_pow2(int v) { return __ffs(v) - 1; }
+
+// Bytes of the receive buffer for clusters of up to MAXKS ranks.
+template <int ROWS, int LD, int MAXKS>
+constexpr int push_recv_bytes() {
+  static_assert(ROWS % MAXKS == 0, "equal slices");
+  return MAXKS > 1 ? (MAXKS - 1) * (ROWS / MAXKS) * LD * 4 : 16;
+}
+
+// Arm the owner's barrier for the ks - 1 incoming slices of its rows
+// (called once, right after mbar_init(bar, 1)).
+template <int ROWS, int LD>
+__device__ __forceinline__ void push_expect(uint64_t *bar, int ks) {
+  const int rows = ROWS >> log2_pow2(ks);
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>((ks - 1) * rows * LD * 4));
+}
+
+// Send every other rank its slice of this rank's parked tile. The tile's
+// writers have fenced their stores to the async proxy and passed a CTA
+// barrier. Slices start on 16-byte boundaries (LD * 4 a multiple of 16).
+template <int ROWS, int LD>
+__device__ __forceinline__ void push_send(const float *red, float *recv, uint64_t *bar, int rank,
+                                          int ks) {
+  const int rows = ROWS >> log2_pow2(ks);
+  for (int r = 0; r < ks; ++r) {
+    if (r == rank) continue;
+    const int k = rank < r ? rank : rank - 1;  // slot of this rank at the owner
+    const uint32_t dst = cluster_map(smem_u32(recv + k * rows * LD), static_cast<uint32_t>(r));
+    const uint32_t rbar = cluster_map(smem_u32(bar), static_cast<uint32_t>(r));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(smem_u32(red + r * rows * LD)), "r"(static_cast<uint32_t>(rows * LD * 4)), "r"(rbar)
+        : "memory");
+  }
+}
+
+// The owner's sum: rows [lo, lo + rows) of the tile, lo = rank * rows, the
+// ks partials (own parked tile for k == rank, receive slot otherwise) added
+// in rank order; y[m0 + m][n0 + row] written for m0 + m < M and
 // n0 + row < N. Consecutive threads take consecutive rows, so the y stores
 // coalesce.
-template <int BM, int LD, int MAXKS>
-__device__ __forceinline__ void split_k_owner_reduce(const float *red, int lo, int my_rows, int ks,
-                                                     int n0, int m0, int M, int N, void *y,
-                                                     int ybf16) {
-  for (int e = threadIdx.x; e < my_rows * (BM / 4); e += blockDim.x) {
-    const int i = e % my_rows, c4 = e / my_rows;
-    const int nl = lo + i;
-    const float *src = red + nl * LD + 4 * c4;
+template <int ROWS, int BM, int LD, int MAXKS>
+__device__ __forceinline__ void push_owner_sum(const float *red, const float *recv, int rank, int ks,
+                                               int n0, int m0, int M, int N, void *y, int ybf16) {
+  const int lrows = log2_pow2(ROWS) - log2_pow2(ks), rows = 1 << lrows;
+  const int lo = rank * rows;
+  for (int e = threadIdx.x; e < rows * (BM / 4); e += blockDim.x) {
+    const int i = e & (rows - 1), c4 = e >> lrows;
     float4 part[MAXKS];
 #pragma unroll
     for (int k = 0; k < MAXKS; ++k)
-      if (k < ks) part[k] = ld_cluster_f32x4(src, static_cast<uint32_t>(k));
+      if (k < ks) {
+        const float *src = k == rank ? red + (lo + i) * LD
+                                     : recv + ((k < rank ? k : k - 1) * rows + i) * LD;
+        part[k] = *reinterpret_cast<const float4 *>(src + 4 * c4);
+      }
     float4 v = part[0];
 #pragma unroll
     for (int k = 1; k < MAXKS; ++k)
       if (k < ks) {
         v.x += part[k].x; v.y += part[k].y; v.z += part[k].z; v.w += part[k].w;
       }
-    if (n0 + nl >= N) continue;
+    if (n0 + lo + i >= N) continue;
     const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int m = 4 * c4 + t;
-      if (m0 + m < M) store_y(y, static_cast<size_t>(m0 + m) * N + n0 + nl, vv[t], ybf16);
+      if (m0 + m < M) store_y(y, static_cast<size_t>(m0 + m) * N + n0 + lo + i, vv[t], ybf16);
     }
   }
 }

@@ -80,9 +80,10 @@ constexpr int FX_ACC = 2;           // group accumulators in TMEM (FX_NB columns
 constexpr int FX_TMEM_COLS = 512;   // the accumulators, then the A ring
 constexpr int FX_A_COL0 = FX_ACC * FX_NB;  // A stage s at column FX_A_COL0 + 32 s
 static_assert(FX_A_COL0 + FX_NS * 32 <= FX_TMEM_COLS, "TMEM budget");
-constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + 1024 + 256;
 constexpr int FX_RED_LD = FX_BM + 4;  // row stride of the parked partial tile (floats)
 constexpr int FX_MAX_KS = 4;          // largest cluster (K split)
+constexpr int FX_RECV_BYTES = push_recv_bytes<FX_ROWS, FX_RED_LD, FX_MAX_KS>();
+constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + FX_RECV_BYTES + 1024 + 256;
 static_assert(FX_ROWS * FX_RED_LD * 4 <= FX_NS * FX_STAGE, "parked partial tile");
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
 // N = 192 (the three 64-row piece tiles are one K-major B tile), M = 128.
@@ -150,14 +151,16 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *xring = smem + NS * SB;                                 // fp32 activation tiles
-  uint64_t *full = reinterpret_cast<uint64_t *>(xring + FX_NSX * FX_X_BYTES);  // A, B written
+  float *recv = reinterpret_cast<float *>(xring + FX_NSX * FX_X_BYTES);  // split-K slices
+  uint64_t *full = reinterpret_cast<uint64_t *>(xring + FX_NSX * FX_X_BYTES + FX_RECV_BYTES);
   uint64_t *xfull = full + NS;                                     // [FX_NSX] tile landed
   uint64_t *xempty = xfull + FX_NSX;                               // [FX_NSX] tile split
   uint64_t *empty = xempty + FX_NSX;                               // MMAs of the stage done
   uint64_t *acc_full = empty + NS;                                 // [FX_ACC] group sum ready
   uint64_t *acc_empty = acc_full + FX_ACC;                         // [FX_ACC] group sum read
   uint64_t *drain = acc_empty + FX_ACC;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *red_bar = drain + 1;  // split-K slices of this rank's rows landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_bar + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -173,8 +176,6 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   const int kb1 = static_cast<int>((static_cast<long long>(nk) * (rank + 1)) / ks);
   const int tile = blockIdx.x;
   const int n0 = tile * FX_ROWS;
-  auto slice_lo = [&](int k) { return (FX_ROWS * k) / ks; };
-  const int my_rows = slice_lo(rank + 1) - slice_lo(rank);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -190,6 +191,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
       mbar_init(&acc_empty[b], FX_RB_WARPS);
     }
     mbar_init(drain, 1);
+    mbar_init(red_bar, 1);
+    if (ks > 1) push_expect<FX_ROWS, FX_RED_LD>(red_bar, ks);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();  // phase A: this rank's barriers are initialised
   const uint32_t tmem = *tmem_slot;
   // Programmatic launch: the weights are read before griddep_wait, x and y
   // after it (no-ops without the launch attribute).
@@ -228,46 +232,57 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
                     &xfull[x]);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int g = 0;  // group counter: buffer g % FX_ACC, use g / FX_ACC
-      bool issued_any = false;
-      for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
-        if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); break; }
-        tc_fence_after();
-        const uint32_t a0 = tmem + FX_A_COL0 + s * 32;  // (nib - 8) in TMEM
-        const uint32_t b0 = smem_u32(smem + s * SB);
-        const int groups = min(2, G32 - 2 * kb);  // the last stage may hold one group
-        bool ok = true;
-        for (int h = 0; h < groups; ++h, ++g) {
-          const int buf = g % FX_ACC;
-          if (!mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(g / FX_ACC) & 1u) ^ 1u) ||
-              aborted(abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // one MMA per 16 columns covers the three pieces: A is read once
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            tc_mma_tmem_a(tmem + buf * FX_NB, a0 + (2 * h + k) * 8,
-                          sw128_desc(b0 + (2 * h + k) * 32), FX_IDESC, k > 0 ? 1u : 0u);
-          tc_commit(&acc_full[buf]);
-          issued_any = true;
+    // the whole warp runs this loop (warp-uniform operands); one elected
+    // lane issues (tc_mma_tmem_a_warp); waits are taken by lane 0 and
+    // broadcast
+    int g = 0;  // group counter: buffer g % FX_ACC, use g / FX_ACC
+    bool issued_any = false;
+    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+      const int s = it % NS;
+      const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&full[s], ph) && !aborted(abort_flag);
+      if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = tmem + FX_A_COL0 + s * 32;  // (nib - 8) in TMEM
+      const uint64_t b0 = sw128_desc(smem_u32(smem + s * SB));
+      const int groups = min(2, G32 - 2 * kb);  // the last stage may hold one group
+      bool ok = true;
+      for (int h = 0; h < groups; ++h, ++g) {
+        const int buf = g % FX_ACC;
+        int free_ = 1;
+        if (lane == 0)
+          free_ = mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(g / FX_ACC) & 1u) ^ 1u) &&
+                  !aborted(abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, free_, 0)) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc_commit(&empty[s]);
+        tc_fence_after();
+        // one MMA per 16 columns covers the three pieces: A is read once
+#pragma unroll
+        for (int k = 0; k < 2; ++k)  // +32 bytes per K step: +2 in the start field
+          tc_mma_tmem_a_warp(tmem + buf * FX_NB, a0 + (2 * h + k) * 8, b0 + 2 * (2 * h + k),
+                             FX_IDESC, k > 0 ? 1u : 0u);
+        tc_commit_warp(&acc_full[buf]);
+        issued_any = true;
       }
-      // every MMA this thread issued is complete before TMEM is released
-      if (issued_any) {
-        tc_commit(drain);
-        mbar_wait(drain, 0);
-      }
+      if (!ok) break;
+      tc_commit_warp(&empty[s]);
     }
+    // every MMA this warp issued is complete before TMEM is released
+    if (issued_any) {
+      tc_commit_warp(drain);
+      if (lane == 0) mbar_wait(drain, 0);
+    }
+    __syncwarp();
   } else if (warp < 2 + FX_DQ_WARPS) {
     // -------------------------------------------------------- dequantisers
     const uint32_t magic = opaque_u32(0x43004300u);  // bf16 pair (128, 128)
@@ -412,22 +427,26 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
 #pragma unroll
       for (int m = 0; m < FX_BM; m += 4)
         *reinterpret_cast<float4 *>(red + m) = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+      fence_proxy_async_smem();  // the bulk copies below read the tile
     }
+    __syncwarp();
   }
 
   __syncthreads();
+  // ------------------------------------------------ split-K reduction (push)
+  // every rank has parked its partial tile (a failed rank sends whatever
+  // its tile holds: the status word already records the failure)
+  cluster_wait();  // phase A: every rank's barriers are initialised
+  const float *red = reinterpret_cast<const float *>(smem);
+  if (threadIdx.x == 0 && ks > 1) push_send<FX_ROWS, FX_RED_LD>(red, recv, red_bar, rank, ks);
   griddep_wait();  // every thread may write y below
-  // ---------------------------------------------------- cluster reduction
-  cluster_sync_all();  // every CTA of the cluster has parked its partial tile
-  {
-    const float *red = reinterpret_cast<const float *>(smem);
-    const bool ok_here = *reinterpret_cast<volatile int *>(abort_flag) == 0;
-    if (ok_here)
-      split_k_owner_reduce<FX_BM, FX_RED_LD, FX_MAX_KS>(red, slice_lo(rank), my_rows, ks, n0, 0,
-                                                        p.M, p.N, p.y, p.ybf16);
-    // no CTA leaves while its shared memory may still be read
-    cluster_sync_all();
-  }
+  if (ks > 1 && !mbar_wait(red_bar, 0)) fail();
+  __syncwarp();
+  cluster_arrive();  // phase B: the slices of this rank's rows have landed
+  if (*reinterpret_cast<volatile int *>(abort_flag) == 0)
+    push_owner_sum<FX_ROWS, FX_BM, FX_RED_LD, FX_MAX_KS>(red, recv, rank, ks, n0, 0, p.M, p.N, p.y,
+                                                         p.ybf16);
+  cluster_wait();  // phase B: every slice this CTA sent has landed
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -473,13 +492,15 @@ cudaError_t launch_tc_f32(const float *x, const int32_t *qw, const float *sc, in
   p.num_tiles = (N + FX_ROWS - 1) / FX_ROWS;
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
-  // split K over a cluster of up to 4 CTAs so that the tiles cover the SMs
-  // once (the fp32 chain of group sums is then at most 128 terms long for
-  // K <= 16384)
+  // split K over a cluster of up to 4 CTAs (a power of two: the split-K
+  // slices are equal) so that the tiles cover the SMs once (the fp32 chain
+  // of group sums is then at most 128 terms long for K <= 16384)
   static const int env_ks = env_int("W4A16_TC_KS");
   const int nk = (K + FX_BK - 1) / FX_BK;
-  const int ks = std::max(1, std::min(std::min(env_ks > 0 ? std::min(env_ks, 4) : 4, nk),
-                                      di.num_sms / std::max(1, p.num_tiles)));
+  const int ks_cap = std::min(std::min(env_ks > 0 ? std::min(env_ks, FX_MAX_KS) : FX_MAX_KS, nk),
+                              di.num_sms / std::max(1, p.num_tiles));
+  int ks = 1;
+  while (2 * ks <= ks_cap) ks *= 2;
   auto kern = tc_f32_kernel;
   static PerDeviceOnce attr_once;
   const cudaError_t attr_err = attr_once.run(

@@ -13,9 +13,10 @@
 // Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: 2-D tiled loads of x (128-byte swizzle) into
 //               the B slot of each pipeline stage;
-//   warp 1      TMEM owner and MMA issuer: one elected thread issues
-//               tcgen05.mma (kind::f16, bf16 x bf16 -> f32) per 16-wide K
-//               step and commits each stage back to its producers;
+//   warp 1      TMEM owner and MMA issuer: the warp runs the issue loop
+//               and one elected lane issues tcgen05.mma (kind::f16, bf16 x
+//               bf16 -> f32) per 16-wide K step and commits each stage back
+//               to its producers;
 //   warps 2-9   dequantisers: thread r owns weight row r of the tile, loads
 //               its packed words and scales straight from global memory,
 //               forms fp32 (nibble - 8) * scale exactly, rounds to bf16 and
@@ -179,45 +180,55 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int it = 0, tcount = 0;
-      bool issued_any = false;
-      for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag);
-           tile += tile_step, ++tcount) {
-        if (tcount > 0 && !mbar_wait(acc_empty, static_cast<uint32_t>(tcount - 1) & 1u)) {
-          fail();
+    // the whole warp runs this loop (warp-uniform operands); one elected
+    // lane issues (tc_mma_warp); waits are taken by lane 0 and broadcast
+    int it = 0, tcount = 0;
+    bool issued_any = false;
+    for (int tile = tile_first; tile < p.num_tiles; tile += tile_step, ++tcount) {
+      int st = 0;  // 1: another warp failed, 2: this wait timed out
+      if (lane == 0) {
+        if (aborted(abort_flag)) st = 1;
+        else if (tcount > 0 && !mbar_wait(acc_empty, static_cast<uint32_t>(tcount - 1) & 1u)) st = 2;
+      }
+      st = __shfl_sync(0xFFFFFFFFu, st, 0);
+      if (st == 2 && lane == 0) fail();
+      if (st != 0) break;
+      tc_fence_after();
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; kb += SK, ++it) {
+        const int s = it % NS;
+        const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
+        const int nsub = min(SK, kb1 - kb);
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&full[s], ph) && !aborted(abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+          if (lane == 0) fail();
+          ok = false;
           break;
         }
         tc_fence_after();
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; kb += SK, ++it) {
-          const int s = it % NS;
-          const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
-          const int nsub = min(SK, kb1 - kb);
-          if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
-          tc_fence_after();
-          for (int j = 0; j < nsub; ++j) {
-            const uint32_t a0 = smem_u32(smem + (s * SK + j) * SB);
-            const uint32_t b0 = a0 + Cfg::kABytes;
+        for (int j = 0; j < nsub; ++j) {
+          const uint32_t a0 = smem_u32(smem + (s * SK + j) * SB);
+          const uint64_t ad = sw128_desc(a0), bd = sw128_desc(a0 + Cfg::kABytes);
 #pragma unroll
-            for (int sub = 0; sub < SUBS; ++sub)
+          for (int sub = 0; sub < SUBS; ++sub)
 #pragma unroll
-              for (int k = 0; k < TC_BK / 16; ++k)
-                tc_mma(tmem + sub * BM, sw128_desc(a0 + sub * A_SUB_BYTES + k * 32),
-                       sw128_desc(b0 + k * 32), Cfg::kIdesc, (kb + j > kb0 || k > 0) ? 1u : 0u);
-          }
-          tc_commit(&empty[s]);
-          issued_any = true;
+            for (int k = 0; k < TC_BK / 16; ++k)  // +32 bytes per K step: +2 in the start field
+              tc_mma_warp(tmem + sub * BM, ad + sub * (A_SUB_BYTES >> 4) + 2 * k, bd + 2 * k,
+                          Cfg::kIdesc, (kb + j > kb0 || k > 0) ? 1u : 0u);
         }
-        if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit_warp(&empty[s]);
+        issued_any = true;
       }
-      // all MMAs this thread issued are complete before TMEM is released
-      if (issued_any) {
-        tc_commit(drain);
-        mbar_wait(drain, 0);
-      }
+      if (!ok) break;
+      tc_commit_warp(acc_full);
     }
+    // all MMAs this warp issued are complete before TMEM is released
+    if (issued_any) {
+      tc_commit_warp(drain);
+      if (lane == 0) mbar_wait(drain, 0);
+    }
+    __syncwarp();
   } else {
     // ---------------------------------------------------- dequant + epilogue
     const NibbleConsts nk = make_nibble_consts();

@@ -17,7 +17,8 @@
 //   warp 0       TMA: one 64 x 64 bf16 activation box (128-byte swizzle)
 //                per block into the stage's B slot;
 //   warp 1       TMEM owner and MMA issuer: per stage, 4 x 4 MMAs
-//                (M=128, N=64, K=16) with A from TMEM, one commit;
+//                (M=128, N=64, K=16) with A from TMEM, one commit, issued
+//                warp-wide by an elected lane;
 //   warps 2-17   dequantisers: warp w handles block (w - 2) / 4 of every
 //                stage for TMEM lane quadrant w % 4; thread = weight row,
 //                8 packed words (64 columns) per block, read from the
@@ -28,10 +29,10 @@
 //                so the weight stream runs ahead with few, large requests.
 // TMEM: columns 0-63 the fp32 accumulator, 64 + 32 * (stage * 4 + block)
 // the A blocks (448 of 512 columns).
-// Epilogue: each rank parks its fp32 partial tile in shared memory; after a
-// cluster barrier the owner of a row slice reads the slice from every rank
-// (distributed shared memory) and adds the partials in rank order, so the
-// result is deterministic and needs no workspace.
+// Epilogue: each rank parks its fp32 partial tile in shared memory and
+// pushes every other rank's row slice to it with one bulk shared -> shared
+// copy; the owner of a slice adds the partials in rank order, so the result
+// is deterministic and needs no workspace (split-K helpers, tc_core.cuh).
 // Every wait is bounded; a timeout is recorded in the status word and the
 // CTA unwinds (TMEM is always freed).
 //
@@ -69,9 +70,10 @@ constexpr int SP_A_COL0 = SP_ACC_COLS;                      // first A block col
 constexpr int SP_TMEM_COLS = 512;
 constexpr int SP_RING_BYTES = SP_NS * SP_SK * SP_B_BYTES;   // 96 KB
 constexpr int SP_WRING_BYTES = SP_NW * SP_W_BYTES;         // 64 KB
-constexpr int SP_SMEM = SP_RING_BYTES + SP_WRING_BYTES + 1024 + 256;
 constexpr int SP_RED_LD = SP_BM + 4;  // row stride of the parked partial tile (floats)
 constexpr int SP_MAX_KS = 8;          // largest cluster (K split)
+constexpr int SP_RECV_BYTES = push_recv_bytes<SP_ROWS, SP_RED_LD, SP_MAX_KS>();
+constexpr int SP_SMEM = SP_RING_BYTES + SP_WRING_BYTES + SP_RECV_BYTES + 1024 + 256;
 static_assert(SP_A_COL0 + SP_NS * SP_SK * 32 <= SP_TMEM_COLS, "TMEM budget");
 static_assert(SP_ROWS * (SP_BM + 4) * 4 <= SP_RING_BYTES, "parked partial tile");
 
@@ -99,13 +101,15 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *wring = smem + SP_RING_BYTES;  // packed weights, 128-byte swizzle
-  uint64_t *full = reinterpret_cast<uint64_t *>(wring + SP_WRING_BYTES);
+  float *recv = reinterpret_cast<float *>(wring + SP_WRING_BYTES);  // split-K slices received
+  uint64_t *full = reinterpret_cast<uint64_t *>(wring + SP_WRING_BYTES + SP_RECV_BYTES);
   uint64_t *empty = full + SP_NS;
   uint64_t *wfull = empty + SP_NS;     // [SP_NW] packed weights landed
   uint64_t *wempty = wfull + SP_NW;    // [SP_NW] packed weights read
   uint64_t *acc_full = wempty + SP_NW;
   uint64_t *drain = acc_full + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *red_bar = drain + 1;       // split-K slices of this rank's rows landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_bar + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,7 +122,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const int tile = blockIdx.x;
   const int n0 = (tile / p.tiles_m) * SP_ROWS;
   const int m0 = (tile % p.tiles_m) * SP_BM;
-  auto slice_lo = [&](int k) { return (SP_ROWS * k) / ks; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SP_NS; ++s) {
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    mbar_init(red_bar, 1);
+    if (ks > 1) push_expect<SP_ROWS, SP_RED_LD>(red_bar, ks);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();  // phase A: this rank's barriers are initialised
   const uint32_t tmem = *tmem_slot;
   // Programmatic launch: the weights are read before griddep_wait (never
   // written by the previous kernel, by the overlap contract), x and y after.
@@ -171,35 +177,43 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                       &full[s]);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int it = 0;
-      bool issued_any = false, ok = true;
-      for (int kb = kb0; kb < kb1; kb += SP_SK, ++it) {
-        const int s = it % SP_NS;
-        const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
-        const int nsub = min(SP_SK, kb1 - kb);
-        if (!mbar_wait(&full[s], ph) || aborted(abort_flag)) { fail(); ok = false; break; }
-        tc_fence_after();
-        for (int j = 0; j < nsub; ++j) {
-          const uint32_t a0 = tmem + SP_A_COL0 + (s * SP_SK + j) * 32;
-          const uint32_t b0 = smem_u32(smem + (s * SP_SK + j) * SP_B_BYTES);
+    // the whole warp runs this loop (warp-uniform operands); one elected
+    // lane issues (tc_mma_tmem_a_warp)
+    int it = 0;
+    bool issued_any = false, ok = true;
+    for (int kb = kb0; kb < kb1; kb += SP_SK, ++it) {
+      const int s = it % SP_NS;
+      const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
+      const int nsub = min(SP_SK, kb1 - kb);
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&full[s], ph) && !aborted(abort_flag);
+      if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+        if (lane == 0) fail();
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int j = 0; j < nsub; ++j) {
+        const uint32_t a0 = tmem + SP_A_COL0 + (s * SP_SK + j) * 32;
+        const uint64_t b0 = sw128_desc(smem_u32(smem + (s * SP_SK + j) * SP_B_BYTES));
 #pragma unroll
-          for (int k = 0; k < SP_BK / 16; ++k)
-            tc_mma_tmem_a(tmem, a0 + k * 8, sw128_desc(b0 + k * 32), SP_IDESC,
-                          (kb + j > kb0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(&empty[s]);
-        issued_any = true;
+        for (int k = 0; k < SP_BK / 16; ++k)  // +32 bytes per K step: +2 in the start field
+          tc_mma_tmem_a_warp(tmem, a0 + k * 8, b0 + 2 * k, SP_IDESC,
+                             (kb + j > kb0 || k > 0) ? 1u : 0u);
       }
-      if (ok) tc_commit(acc_full);
-      // all MMAs this thread issued are complete before TMEM is released
-      if (issued_any) {
-        tc_commit(drain);
-        mbar_wait(drain, 0);
-      }
+      tc_commit_warp(&empty[s]);
+      issued_any = true;
     }
+    if (ok) tc_commit_warp(acc_full);
+    // all MMAs this warp issued are complete before TMEM is released
+    if (issued_any) {
+      tc_commit_warp(drain);
+      if (lane == 0) mbar_wait(drain, 0);
+    }
+    __syncwarp();
   } else if (warp == SP_WP_WARP) {
     // ------------------------------------------------- weight producer (TMA)
     // one 128-row x 32-word box per stage (the 4 blocks' packed words;
@@ -215,6 +229,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         tma_load_2d(wring + ws * SP_W_BYTES, &tmap_w, kb * 8, n0, &wfull[ws]);
       }
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------- dequantisers
     const NibbleConsts nk_ = make_nibble_consts();
@@ -306,25 +321,28 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
               *reinterpret_cast<uint4 *>(red + cc * 32 + t) =
                   make_uint4(r[t], r[t + 1], r[t + 2], r[t + 3]);
           }
+          fence_proxy_async_smem();  // the bulk copies below read the tile
         }
       }
     }
     tc_fence_before();
+    __syncwarp();
   }
   __syncthreads();
-  // every CTA of the cluster has parked its partial tile (or failed)
-  cluster_sync_all();
+  // ------------------------------------------------ split-K reduction (push)
+  // every rank has parked its partial tile (a failed rank sends whatever
+  // its tile holds: the status word already records the failure)
+  cluster_wait();  // phase A: every rank's barriers are initialised
+  const float *red = reinterpret_cast<const float *>(smem);
+  if (threadIdx.x == 0 && ks > 1) push_send<SP_ROWS, SP_RED_LD>(red, recv, red_bar, rank, ks);
   griddep_wait();  // every thread may write y below
-  {
-    const bool ok_all = *reinterpret_cast<volatile int *>(abort_flag) == 0;
-    const int lo = slice_lo(rank), my_rows = slice_lo(rank + 1) - lo;
-    const float *red = reinterpret_cast<const float *>(smem);
-    if (ok_all)
-      split_k_owner_reduce<SP_BM, SP_RED_LD, SP_MAX_KS>(red, lo, my_rows, ks, n0, m0, p.M, p.N,
-                                                        p.y, p.ybf16);
-  }
-  // no CTA leaves while its shared memory may still be read
-  cluster_sync_all();
+  if (ks > 1 && !mbar_wait(red_bar, 0)) fail();
+  __syncwarp();
+  cluster_arrive();  // phase B: the slices of this rank's rows have landed
+  if (*reinterpret_cast<volatile int *>(abort_flag) == 0)
+    push_owner_sum<SP_ROWS, SP_BM, SP_RED_LD, SP_MAX_KS>(red, recv, rank, ks, n0, m0, p.M, p.N,
+                                                         p.y, p.ybf16);
+  cluster_wait();  // phase B: every slice this CTA sent has landed
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
