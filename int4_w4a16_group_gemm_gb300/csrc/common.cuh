@@ -109,6 +109,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, for a waiter with slack: polls without suspending and
+// sleeps about `sleep_ns` between polls, so that while it waits it takes
+// (almost) no issue slots from the warps on its scheduler. Meant for one
+// lane per warp.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity,
+                                                  uint32_t sleep_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // As mbar_wait, but also gives up (returning false) once `*abort` becomes
 // nonzero: another warp of the CTA has already timed out, so the phase may
 // never complete. The flag is polled between batches of try_waits.

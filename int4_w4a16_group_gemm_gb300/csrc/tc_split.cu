@@ -13,7 +13,8 @@
 // tcgen05.mma); shared memory only carries the activations (TMA).
 //
 // Tile: 128 weight rows x 64 tokens, K split over a cluster of ks CTAs
-// (grid y = rank). Pipeline stage = 4 blocks of 64 K columns, 3 stages:
+// (grid y = rank) at whole stages. Pipeline stage = 4 blocks of 64 K
+// columns, 3 stages:
 //   warp 0       TMA: one 64 x 64 bf16 activation box (128-byte swizzle)
 //                per block into the stage's B slot;
 //   warp 1       TMEM owner and MMA issuer: per stage, 4 x 4 MMAs
@@ -21,12 +22,16 @@
 //                warp-wide by an elected lane;
 //   warps 2-17   dequantisers: warp w handles block (w - 2) / 4 of every
 //                stage for TMEM lane quadrant w % 4; thread = weight row,
-//                8 packed words (64 columns) per block, read from the
-//                weight ring, dequantised to bf16 pairs and stored as 32
-//                TMEM columns;
+//                8 packed words (64 columns) per block and the row's two
+//                group scales, read from the weight ring, dequantised to
+//                bf16 pairs and stored as 32 TMEM columns;
 //   warp 18      weight producer: one TMA box of the stage's packed words
-//                (128 rows x 128 bytes, 128-byte swizzle) into a ring of 4,
-//                so the weight stream runs ahead with few, large requests.
+//                (128 rows x 128 bytes, 128-byte swizzle) and one of its
+//                scales (128 rows x 8 or 4 floats) into a ring of 4, so the
+//                weight stream runs ahead with few, large requests. (When
+//                a scale row is not a whole number of 16-byte units the
+//                dequantisers load their scales themselves, two stages
+//                ahead.)
 // TMEM: columns 0-63 the fp32 accumulator, 64 + 32 * (stage * 4 + block)
 // the A blocks (448 of 512 columns).
 // Epilogue: each rank parks its fp32 partial tile in shared memory and
@@ -64,18 +69,24 @@ constexpr int SP_WP_WARP = 2 + SP_DQ_WARPS;  // the weight producer (TMA)
 constexpr int SP_THREADS = 96 + 32 * SP_DQ_WARPS;
 constexpr int SP_NW = 4;           // stages of packed weights in shared memory
 constexpr int SP_W_BYTES = SP_ROWS * SP_SK * 32;  // 128 rows x 128 B per stage
+// scales of a stage (scales by TMA): 128 rows x SCB floats, SCB = 8 for
+// groups of 32 (the stage's 8 groups), 4 otherwise (an aligned window that
+// holds the stage's 4, 2 groups)
+constexpr int SP_SC_BYTES = SP_ROWS * 8 * 4;
+constexpr int SP_WSLOT = SP_W_BYTES + SP_SC_BYTES;  // one weight-ring slot
 constexpr int SP_B_BYTES = SP_BM * SP_BK * 2;               // 8 KB per block
 constexpr int SP_ACC_COLS = SP_BM;                          // fp32 accumulator
 constexpr int SP_A_COL0 = SP_ACC_COLS;                      // first A block column
 constexpr int SP_TMEM_COLS = 512;
 constexpr int SP_RING_BYTES = SP_NS * SP_SK * SP_B_BYTES;   // 96 KB
-constexpr int SP_WRING_BYTES = SP_NW * SP_W_BYTES;         // 64 KB
+constexpr int SP_WRING_BYTES = SP_NW * SP_WSLOT;           // 80 KB
 constexpr int SP_RED_LD = SP_BM + 4;  // row stride of the parked partial tile (floats)
 constexpr int SP_MAX_KS = 8;          // largest cluster (K split)
 constexpr int SP_RECV_BYTES = push_recv_bytes<SP_ROWS, SP_RED_LD, SP_MAX_KS>();
 constexpr int SP_SMEM = SP_RING_BYTES + SP_WRING_BYTES + SP_RECV_BYTES + 1024 + 256;
 static_assert(SP_A_COL0 + SP_NS * SP_SK * 32 <= SP_TMEM_COLS, "TMEM budget");
 static_assert(SP_ROWS * (SP_BM + 4) * 4 <= SP_RING_BYTES, "parked partial tile");
+static_assert(SP_WSLOT % 1024 == 0, "weight slots keep the 128-byte swizzle atoms aligned");
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
 // N = 64, M = 128.
@@ -89,14 +100,22 @@ struct SpParams {
   void *y;  // fp32, or bf16 when ybf16
   int ybf16;
   int M, N, K;
-  int tiles_m, num_tiles;
-  int gs;  // log2 of the group size
+  int gs;   // log2 of the group size
+  int lks;  // log2 of the K split (cluster size)
+  int scb;  // floats per row in a stage's scale box (scales by TMA)
   int *status;
 };
 
+// SCT: the scales come by TMA with the packed words (a box of 128 rows x
+// scb floats per stage); otherwise each dequantiser thread loads its row's
+// scales from global memory two stages ahead (the scale rows must then
+// have a 16-byte multiple stride for the tensor map, K / group % 4 == 0).
+// Grid: x = weight-row tile, y = K rank (the cluster), z = token tile.
+template <bool SCT>
 __global__ void __launch_bounds__(SP_THREADS, 1)
     tc_split_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                    const __grid_constant__ CUtensorMap tmap_w, const SpParams p) {
+                    const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_s, const SpParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -104,7 +123,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   float *recv = reinterpret_cast<float *>(wring + SP_WRING_BYTES);  // split-K slices received
   uint64_t *full = reinterpret_cast<uint64_t *>(wring + SP_WRING_BYTES + SP_RECV_BYTES);
   uint64_t *empty = full + SP_NS;
-  uint64_t *wfull = empty + SP_NS;     // [SP_NW] packed weights landed
+  uint64_t *wfull = empty + SP_NS;     // [SP_NW] packed weights (and scales) landed
   uint64_t *wempty = wfull + SP_NW;    // [SP_NW] packed weights read
   uint64_t *acc_full = wempty + SP_NW;
   uint64_t *drain = acc_full + 1;
@@ -115,13 +134,15 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   const int nk = (K + SP_BK - 1) / SP_BK;
+  // K is split at whole stages: rank r takes stages [nst r / ks, nst (r+1) / ks)
+  // (the launcher keeps ks <= nst, so every rank has at least one)
+  const int nst = (nk + SP_SK - 1) / SP_SK;
   const int rank = static_cast<int>(blockIdx.y);
-  const int ks = static_cast<int>(gridDim.y);
-  const int kb0 = static_cast<int>((static_cast<long long>(nk) * rank) / ks);
-  const int kb1 = static_cast<int>((static_cast<long long>(nk) * (rank + 1)) / ks);
-  const int tile = blockIdx.x;
-  const int n0 = (tile / p.tiles_m) * SP_ROWS;
-  const int m0 = (tile % p.tiles_m) * SP_BM;
+  const int ks = 1 << p.lks;
+  const int kb0 = ((nst * rank) >> p.lks) * SP_SK;
+  const int kb1 = min(nk, ((nst * (rank + 1)) >> p.lks) * SP_SK);
+  const int n0 = static_cast<int>(blockIdx.x) * SP_ROWS;
+  const int m0 = static_cast<int>(blockIdx.z) * SP_BM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SP_NS; ++s) {
@@ -169,7 +190,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         const int s = it % SP_NS;
         const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
         const int nsub = min(SP_SK, kb1 - kb);
-        if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
+        if (!mbar_wait_backoff(&empty[s], ph ^ 1u, 32)) { fail(); break; }
         if (aborted(abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * SP_B_BYTES));
         for (int j = 0; j < nsub; ++j)
@@ -217,16 +238,24 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   } else if (warp == SP_WP_WARP) {
     // ------------------------------------------------- weight producer (TMA)
     // one 128-row x 32-word box per stage (the 4 blocks' packed words;
-    // words past K read as zero), 128-byte swizzle; runs SP_NW stages ahead
+    // words past K read as zero), 128-byte swizzle, and with SCT the
+    // stage's scale box; runs SP_NW stages ahead
     if (lane == 0) {
       int it = 0;
       for (int kb = kb0; kb < kb1 && !aborted(abort_flag); kb += SP_SK, ++it) {
         const int ws = it % SP_NW;
         const uint32_t ph = static_cast<uint32_t>(it / SP_NW) & 1u;
-        if (!mbar_wait(&wempty[ws], ph ^ 1u)) { fail(); break; }
+        if (!mbar_wait_backoff(&wempty[ws], ph ^ 1u, 32)) { fail(); break; }
         if (aborted(abort_flag)) break;
-        mbar_arrive_expect_tx(&wfull[ws], SP_W_BYTES);
-        tma_load_2d(wring + ws * SP_W_BYTES, &tmap_w, kb * 8, n0, &wfull[ws]);
+        uint8_t *slot = wring + ws * SP_WSLOT;
+        if constexpr (SCT) {
+          // the stage's scales: groups from ((kb * 64) >> gs) aligned down to 4
+          mbar_arrive_expect_tx(&wfull[ws], SP_W_BYTES + SP_ROWS * p.scb * 4);
+          tma_load_2d(slot + SP_W_BYTES, &tmap_s, ((kb * SP_BK) >> p.gs) & ~3, n0, &wfull[ws]);
+        } else {
+          mbar_arrive_expect_tx(&wfull[ws], SP_W_BYTES);
+        }
+        tma_load_2d(slot, &tmap_w, kb * 8, n0, &wfull[ws]);
       }
     }
     __syncwarp();
@@ -243,10 +272,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const int G = K >> p.gs;
     const float *srow = p.sc + static_cast<size_t>(nvalid ? n : 0) * G;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    // this row's two scales of block kb (0 past K or N)
+    // this row's two scales of block kb (0 past K or N), from global memory
     auto fetch_sc = [&](int kb, float (&sc)[2]) {
       sc[0] = sc[1] = 0.f;
-      if (!nvalid || kb >= kb1) return;
+      if (SCT || !nvalid || kb >= kb1) return;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int w0 = kb * 8 + 4 * h;
@@ -272,16 +301,30 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         const uint32_t ph = static_cast<uint32_t>(it / SP_NS) & 1u;
         const uint32_t wph = static_cast<uint32_t>(it / SP_NW) & 1u;
         ++it;
-        const float cs[2] = {rsc[u][0], rsc[u][1]};
+        float cs[2] = {rsc[u][0], rsc[u][1]};
         fetch_sc(kbs + 2 * SP_SK + j, rsc[u]);
         // the packed words have landed, then the TMEM slot is free
-        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&wfull[ws], wph) &&
-                                                     mbar_wait(&empty[s], ph ^ 1u) &&
-                                                     !aborted(abort_flag));
+        // (one lane waits, sleeping between polls: these warps run ahead of
+        // the MMA warp, which shares their schedulers)
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait_backoff(&wfull[ws], wph, 32) &&
+                mbar_wait_backoff(&empty[s], ph ^ 1u, 32) && !aborted(abort_flag);
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        __syncwarp();  // orders lane 0's acquire before the other lanes' reads
         if (!got) { fail(); ok = false; break; }
-        const uint8_t *wst = wring + ws * SP_W_BYTES;
+        const uint8_t *wst = wring + ws * SP_WSLOT;
         const uint4 c0 = *reinterpret_cast<const uint4 *>(wst + woff0);
         const uint4 c1 = *reinterpret_cast<const uint4 *>(wst + woff1);
+        if constexpr (SCT) {
+          // block kbs + j, halves h: group ((kbs + j) * 64 + 32 h) >> gs,
+          // at its offset in the stage's aligned window of groups
+          const float *srow_s = reinterpret_cast<const float *>(wst + SP_W_BYTES) + row * p.scb;
+          const int c0g = ((kbs * SP_BK) >> p.gs) & ~3;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            cs[h] = srow_s[((((kbs + j) * SP_BK) + 32 * h) >> p.gs) - c0g];
+        }
         tc_fence_after();
         if (kbs + j < kb1) {
           uint32_t a[32];
@@ -387,38 +430,57 @@ cudaError_t launch_tc_split(const uint16_t *x, const int32_t *qw, const float *s
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_m = (M + SP_BM - 1) / SP_BM;
-  p.num_tiles = p.tiles_m * ((N + SP_ROWS - 1) / SP_ROWS);
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
+  p.scb = group == 32 ? 8 : 4;
   p.status = di.status;
-  // split K over a cluster of up to kmax CTAs (a power of two) so that the
-  // clusters cover the SMs once
-  const int nk = (K + SP_BK - 1) / SP_BK;
-  int ks = 1;
-  while (2 * ks <= std::min(std::min(std::min(kmax, SP_MAX_KS), nk),
-                            di.num_sms / std::max(1, p.num_tiles)))
-    ks *= 2;
+  // scales [N][K/group] fp32 by TMA when a scale row is a whole number of
+  // 16-byte units: a box of scb floats x 128 rows per stage, zeros past the
+  // row's end and past N (an aligned window of 4 groups holds a stage's 2
+  // groups of 128 columns; with groups of 32 a stage starts on a multiple
+  // of 8 groups, with 64 on a multiple of 4)
+  const int G = K / group;
+  const bool sct = G % 4 == 0 && (reinterpret_cast<uintptr_t>(sc) & 15u) == 0;
+  CUtensorMap tmap_s = tmap_w;
+  if (sct) {
+    const cuuint64_t sdims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(N)};
+    const cuuint64_t sstrides[1] = {static_cast<cuuint64_t>(G) * 4};
+    const cuuint32_t sbox[2] = {static_cast<cuuint32_t>(p.scb), SP_ROWS};
+    r = encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(sc), sdims, sstrides,
+               sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  const int tiles_m = (M + SP_BM - 1) / SP_BM;
+  const int tiles_n = (N + SP_ROWS - 1) / SP_ROWS;
+  // split K over a cluster of up to kmax CTAs (a power of two, at most the
+  // number of stages) so that the clusters cover the SMs once
+  const int nst = (K + SP_BK * SP_SK - 1) / (SP_BK * SP_SK);
+  int lks = 0;
+  while ((2 << lks) <= std::min(std::min(std::min(kmax, SP_MAX_KS), nst),
+                                di.num_sms / std::max(1, tiles_m * tiles_n)))
+    ++lks;
+  p.lks = lks;
 
-  auto kern = tc_split_kernel;
-  static PerDeviceOnce attr_once;
-  const cudaError_t attr_err = attr_once.run(
+  auto kern = sct ? tc_split_kernel<true> : tc_split_kernel<false>;
+  static PerDeviceOnce attr_once[2];
+  const cudaError_t attr_err = attr_once[sct ? 1 : 0].run(
       [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM); });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_tiles, ks);
+  cfg.gridDim = dim3(tiles_n, 1 << lks, tiles_m);
   cfg.blockDim = dim3(SP_THREADS);
   cfg.dynamicSmemBytes = SP_SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = ks;
+  attr[0].val.clusterDim.y = 1 << lks;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, tmap_s, p);
 }
 
 }  // namespace w4a16
