@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       griddep_wait();
+      // the activation tiles are re-read by every weight tile of their token
+      // tile, in later waves too: keep them in L2 ahead of the weights and
+      // the output stream
+      const uint64_t keep = l2_policy_evict_last();
       int it = 0;
       for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag); tile += tile_step) {
         const int m0 = (tile % p.tiles_m) * BM;
@@ -173,8 +177,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           if (aborted(abort_flag)) break;
           mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * Cfg::kBBytes));
           for (int j = 0; j < nsub; ++j)
-            tma_load_2d(smem + (s * SK + j) * SB + Cfg::kABytes, &tmap_x, (kb + j) * TC_BK, m0,
-                        &full[s]);
+            tma_load_2d_hint(smem + (s * SK + j) * SB + Cfg::kABytes, &tmap_x, (kb + j) * TC_BK,
+                             m0, &full[s], keep);
         }
       }
     }
