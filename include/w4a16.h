@@ -61,7 +61,10 @@ typedef enum {
                                 kernel limit */
   W4A16_ERR_ALIGNMENT = 3,   /* a pointer not 16-byte aligned */
   W4A16_ERR_CUDA = 4,        /* a CUDA runtime or launch error */
-  W4A16_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out */
+  W4A16_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out */
+  W4A16_ERR_BOUNDS = 6       /* bounds-checking build only (compiled with
+                                W4A16_DEBUG): a kernel computed an index
+                                outside its buffer and skipped the access */
 } w4a16_status;
 
 typedef enum {

@@ -30,7 +30,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libw4a16.so")
+# W4A16_LIBRARY selects another build of the library (the bounds-checking
+# build, libw4a16_debug.so); by default the release build next to this file.
+LIB_PATH = os.environ.get("W4A16_LIBRARY") or os.path.join(HERE, "libw4a16.so")
 
 W4A16_OK = 0
 W4A16_ERR_INVALID_ARG = 1
@@ -38,6 +40,7 @@ W4A16_ERR_UNSUPPORTED = 2
 W4A16_ERR_ALIGNMENT = 3
 W4A16_ERR_CUDA = 4
 W4A16_ERR_TIMEOUT = 5
+W4A16_ERR_BOUNDS = 6
 
 ACT_F32 = 0
 ACT_BF16 = 1

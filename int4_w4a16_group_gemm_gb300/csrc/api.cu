@@ -337,6 +337,7 @@ const char *w4a16_status_string(w4a16_status s) {
     case W4A16_ERR_ALIGNMENT: return "W4A16_ERR_ALIGNMENT";
     case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
     case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+    case W4A16_ERR_BOUNDS: return "W4A16_ERR_BOUNDS";
   }
   return "W4A16_ERR_UNKNOWN";
 }

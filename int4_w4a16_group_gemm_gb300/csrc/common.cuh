@@ -17,6 +17,20 @@ __device__ __forceinline__ void record_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Bounds checks of the W4A16_DEBUG build: W4A16_IN_BOUNDS(cond, status)
+// is true when the access it guards stays inside its buffer; otherwise it
+// records W4A16_ERR_BOUNDS in the status word and is false, so the caller
+// skips the access. In the release build it is `true` and compiles away.
+#ifdef W4A16_DEBUG
+__device__ __forceinline__ bool w4a16_in_bounds(bool ok, int *status) {
+  if (!ok) record_status(status, W4A16_ERR_BOUNDS);
+  return ok;
+}
+#define W4A16_IN_BOUNDS(cond, status) (::w4a16::w4a16_in_bounds((cond), (status)))
+#else
+#define W4A16_IN_BOUNDS(cond, status) true
+#endif
+
 // Wall-clock bound for every spin-wait, in nanoseconds (~1 s).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

@@ -145,6 +145,9 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_kernel(const GemvParams p)
     uint8_t *dst = stages + slot * stage_bytes;
     const uint32_t bq = rows * qrow, bs = rows * srow;
     sh.slot_stage[slot] = s;
+    // rows [row, row + rows) of qw and sc, into a stage of RS rows
+    if (!W4A16_IN_BOUNDS(row >= 0 && rows > 0 && rows <= RS && row + rows <= p.N, p.status))
+      return;  // the stage never fills: its waits time out
     mbar_arrive_expect_tx(&sh.full[slot], bq + bs);
     bulk_g2s(dst, reinterpret_cast<const uint8_t *>(p.qw) + static_cast<size_t>(row) * qrow, bq,
              &sh.full[slot]);
@@ -231,8 +234,9 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_kernel(const GemvParams p)
     uint64_t xp[8];
     {
       float x0[8], x1[8];
-      load_x8<BF16>(p.x, wc * 8, active, x0);
-      load_x8<BF16>(p.x, wc * 8 + 8, active, x1);
+      const bool xin = W4A16_IN_BOUNDS(!active || wc * 8 + 16 <= p.K, p.status);
+      load_x8<BF16>(p.x, wc * 8, active && xin, x0);
+      load_x8<BF16>(p.x, wc * 8 + 8, active && xin, x1);
 #pragma unroll
       for (int j = 0; j < 8; ++j) xp[j] = pack_f32x2(x0[j], x1[j]);
     }
@@ -268,7 +272,8 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_kernel(const GemvParams p)
     uint64_t xd[8];
     {
       float x0[8];
-      load_x8<BF16>(p.x, wc * 8, active, x0);
+      const bool xin = W4A16_IN_BOUNDS(!active || wc * 8 + 8 <= p.K, p.status);
+      load_x8<BF16>(p.x, wc * 8, active && xin, x0);
 #pragma unroll
       for (int j = 0; j < 8; ++j) xd[j] = pack_f32x2(x0[j], x0[j]);
     }
@@ -316,7 +321,8 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_kernel(const GemvParams p)
     float a = 0.f;
 #pragma unroll
     for (int w = 0; w < kGvWarps; ++w) a += v[w];
-    store_y(p.y, static_cast<size_t>(r0 + threadIdx.x), a, p.ybf16);
+    if (W4A16_IN_BOUNDS(r0 + static_cast<int>(threadIdx.x) < p.N, p.status))
+      store_y(p.y, static_cast<size_t>(r0 + threadIdx.x), a, p.ybf16);
   }
 }
 

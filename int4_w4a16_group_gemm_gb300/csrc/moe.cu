@@ -144,6 +144,7 @@ struct MoeParams {
   const float *sc;
   void *out;              // gate/up: h [n][I]; down: o [n][H] fp32 (by pair)
   int H, I, topk;
+  int n_pairs, E;  // buffer extents for the bounds-checking build
   int nstages;
   int gs;       // log2 of the group size
   int srow;     // bytes per scale row: (K / group) * 4, K the reduced dimension
@@ -183,8 +184,10 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
   const int it = blockIdx.x;
   if (it >= *p.n_items) return;  // the grid is sized for the most items
   const int e = p.items[2 * it];
+  if (!W4A16_IN_BOUNDS(e >= 0 && e < p.E, p.status)) return;
   const int s0 = p.offsets[e] + p.items[2 * it + 1] * MT;
   const int mt = min(MT, p.offsets[e + 1] - s0);
+  if (!W4A16_IN_BOUNDS(s0 >= 0 && s0 + mt <= p.n_pairs, p.status)) return;
 
   const int K = MODE == 0 ? p.H : p.I;
   const int L = MODE == 0 ? p.I : p.H;  // logical rows of the expert
@@ -229,6 +232,9 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
     uint8_t *dst = stages + slot * stage_bytes;
     const int parts = MODE == 0 ? 2 : 1;
     const uint32_t bq = rows * qrow, bs = p.sc_bulk ? rows * srow : 0u;
+    // rows [l0, l0 + rows) (and the matching up rows) of this expert
+    if (!W4A16_IN_BOUNDS(l0 >= 0 && rows > 0 && l0 + rows <= L, p.status))
+      return;  // the stage never fills: its waits time out
     mbar_arrive_expect_tx(&full[slot], parts * (bq + bs));
     for (int h = 0; h < parts; ++h) {
       const size_t grow = static_cast<size_t>(l0) + (h ? p.I : 0);
@@ -281,7 +287,9 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 #pragma unroll
       for (int t = 0; t < TM; ++t) {
         const void *row = nullptr;
-        if (active && t < mt) {
+        if (active && t < mt &&
+            W4A16_IN_BOUNDS(k0 + EPL <= K && p.perm[s0 + t] >= 0 && p.perm[s0 + t] < p.n_pairs,
+                            p.status)) {
           const int s = s0 + t;
           const size_t xrow = MODE == 0 ? static_cast<size_t>(p.perm[s] / p.topk) * p.H
                                         : static_cast<size_t>(s) * p.I;
@@ -297,7 +305,10 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 #pragma unroll
           for (int r = 0; r < RC; ++r) {
             const int grow = stage_row(c, r);
-            sv[r] = grow >= 0 ? __ldg(reinterpret_cast<const float *>(
+            sv[r] = grow >= 0 && W4A16_IN_BOUNDS(static_cast<size_t>(grow) < erows &&
+                                                     g < (K >> p.gs),
+                                                 p.status)
+                        ? __ldg(reinterpret_cast<const float *>(
                                           sbase + static_cast<size_t>(grow) * srow) + g)
                               : 0.f;
           }
@@ -350,6 +361,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
   for (int i = threadIdx.x; i < nl * MT; i += blockDim.x) {
     const int l = i / MT, t = i - l * MT;
     if (t >= mt) continue;
+    if (!W4A16_IN_BOUNDS(l_begin + l < L, p.status)) continue;
     if (MODE == 0) {
       const int prow = (l / 4) * RC + (l & 3);
       const float h = silu_f(rowsum(prow, t)) * rowsum(prow + 4, t);
@@ -360,6 +372,7 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
         static_cast<float *>(p.out)[idx] = h;
     } else {
       const int pair = p.perm[s0 + t];
+      if (!W4A16_IN_BOUNDS(pair >= 0 && pair < p.n_pairs, p.status)) continue;
       static_cast<float *>(p.out)[static_cast<size_t>(pair) * p.H + l_begin + l] =
           p.route_w[pair] * rowsum(l, t);
     }
@@ -369,9 +382,10 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) moe_expert_kernel(const MoePa
 // ------------------------------------------------------------------ 4. combine
 __global__ void moe_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
                                    const float *__restrict__ shared, int T, int topk, int H,
-                                   int E, float *__restrict__ y) {
+                                   int E, float *__restrict__ y, int *status) {
   const int H4 = H >> 2;
   const long long total = static_cast<long long>(T) * H4;
+  if (!W4A16_IN_BOUNDS(H % 4 == 0, status)) return;  // 16-byte rows
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / H4);
@@ -529,6 +543,8 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
   p.H = H;
   p.I = I;
   p.topk = topk;
+  p.n_pairs = n;
+  p.E = E;
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
 
@@ -548,7 +564,8 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
 
   const long long work = static_cast<long long>(T) * (H / 4);
   const int grid = static_cast<int>(std::min<long long>((work + 255) / 256, di.num_sms * 8ll));
-  moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, shared_o, T, topk, H, E, y);
+  moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, shared_o, T, topk, H, E, y,
+                                                            di.status);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ constexpr int kRtWarps = 4;
 template <bool BF16>
 __global__ void __launch_bounds__(32 * kRtWarps)
     router_logits_kernel(const void *__restrict__ x, const float *__restrict__ wr, int T, int H,
-                         int E, int tiles_e, int tiles, float *__restrict__ logits) {
+                         int E, int tiles_e, int tiles, float *__restrict__ logits, int *status) {
   __shared__ float red[kRtWarps][kRtTok * kRtExp][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x * kRtWarps + warp;
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(32 * kRtWarps)
     for (int e = 0; e < kRtExp; ++e) acc[t][e] = 0.f;
 
   for (int k = lane * 4; k < H; k += 128) {
+    if (!W4A16_IN_BOUNDS(k + 4 <= H, status)) break;  // 4 columns per 16-byte load
     float4 xv[kRtTok];
 #pragma unroll
     for (int t = 0; t < kRtTok; ++t) {
@@ -107,7 +108,7 @@ template <int NPL>
 __global__ void __launch_bounds__(256)
     router_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
                        int E, int topk, float scale, int32_t *__restrict__ ids,
-                       float *__restrict__ route_w) {
+                       float *__restrict__ route_w, int *status) {
   const int lane = threadIdx.x & 31;
   const int t = static_cast<int>((blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x) >> 5);
   if (t >= T) return;
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(256)
     }
     sum += bs;  // the same slot order on every lane
   }
-  if (lane < topk) {
+  if (lane < topk && W4A16_IN_BOUNDS(my_id >= 0 && my_id < E, status)) {
     ids[static_cast<size_t>(t) * topk + lane] = my_id;
     route_w[static_cast<size_t>(t) * topk + lane] = scale * my_s / sum;
   }
@@ -185,7 +186,7 @@ template <int NPL>
 cudaError_t launch_topk(const float *logits, const float *bias, int T, int E, int topk,
                         float scale, int32_t *ids, float *route_w, cudaStream_t stream) {
   router_topk_kernel<NPL><<<(T + 7) / 8, 256, 0, stream>>>(logits, bias, T, E, topk, scale, ids,
-                                                          route_w);
+                                                          route_w, device_info().status);
   return cudaGetLastError();
 }
 
@@ -199,10 +200,11 @@ cudaError_t launch_router(const void *x, bool x_bf16, int T, int H, const float 
   const int grid = (tiles + kRtWarps - 1) / kRtWarps;
   if (x_bf16)
     router_logits_kernel<true><<<grid, 32 * kRtWarps, 0, stream>>>(x, router_w, T, H, E, tiles_e,
-                                                                   tiles, logits);
+                                                                   tiles, logits, device_info().status);
   else
     router_logits_kernel<false><<<grid, 32 * kRtWarps, 0, stream>>>(x, router_w, T, H, E,
-                                                                    tiles_e, tiles, logits);
+                                                                    tiles_e, tiles, logits,
+                                                                    device_info().status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (E <= 128) return launch_topk<4>(logits, bias, T, E, topk, scale, ids, route_w, stream);

@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     uint8_t *dst = stages + slot * stage_bytes;
     const uint32_t bq = rows * qrow;
     const uint32_t bs = SCB ? rows * srow : 0u;
+    // rows [row, row + rows) of qw and sc, into a stage of RC rows
+    if (!W4A16_IN_BOUNDS(row >= 0 && rows > 0 && rows <= RC && row + rows <= p.N, p.status))
+      return;  // the stage never fills: its waits time out
     mbar_arrive_expect_tx(&full[slot], bq + bs);
     bulk_g2s(dst, reinterpret_cast<const uint8_t *>(p.qw) + static_cast<size_t>(row) * qrow, bq,
              &full[slot]);
@@ -149,11 +152,16 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     const bool active = k0 < K;
     const int kc = active ? k0 : 0;  // inactive lanes read valid smem, weigh zero
     const int g = kc >> p.gs;  // a lane's columns lie in one group
+    // this lane's words and scale inside every stage row
+    (void)W4A16_IN_BOUNDS((kc >> 1) + 4 * WPL <= static_cast<int>(qrow) &&
+                              (!SCB || g * 4 < static_cast<int>(srow)),
+                          p.status);
     uint64_t xr[MT][EPL / 2];
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       const void *xrow = nullptr;
-      if (active && t < mt) {
+      if (active && t < mt &&
+          W4A16_IN_BOUNDS(m0 + t < p.M && k0 + EPL <= p.K && p.ldx >= p.K, p.status)) {
         const size_t off = static_cast<size_t>(m0 + t) * p.ldx;
         xrow = BF16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.x) + off)
                     : static_cast<const void *>(static_cast<const float *>(p.x) + off);
@@ -171,10 +179,11 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
         const int rows = min(RC, r1 - row0);
 #pragma unroll
         for (int r = 0; r < RC; ++r)
-          sv[r] = r < rows ? __ldg(reinterpret_cast<const float *>(
-                                     reinterpret_cast<const uint8_t *>(p.sc) +
-                                     static_cast<size_t>(row0 + r) * srow) + g)
-                           : 0.f;
+          sv[r] = r < rows && W4A16_IN_BOUNDS(row0 + r < p.N && g < (K >> p.gs), p.status)
+                      ? __ldg(reinterpret_cast<const float *>(
+                                  reinterpret_cast<const uint8_t *>(p.sc) +
+                                  static_cast<size_t>(row0 + r) * srow) + g)
+                      : 0.f;
       }
       int ok = 1;
       if (lane == 0) {
@@ -246,7 +255,8 @@ __global__ void __launch_bounds__(32 * MAXW, MINB) stream_gemm_kernel(const Stre
     const float *v = red + static_cast<size_t>(i) * nw;
     float a = 0.f;
     for (int w = 0; w < nw; ++w) a += v[w];
-    store_y(p.y, static_cast<size_t>(m0 + t) * p.ldy + r0 + row, a, p.ybf16);
+    if (W4A16_IN_BOUNDS(m0 + t < p.M && r0 + row < p.N && p.ldy >= p.N, p.status))
+      store_y(p.y, static_cast<size_t>(m0 + t) * p.ldy + r0 + row, a, p.ybf16);
   }
 }
 

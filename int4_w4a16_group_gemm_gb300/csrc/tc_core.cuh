@@ -292,7 +292,8 @@ __device__ __forceinline__ void push_send(const float *red, float *recv, uint64_
 // coalesce.
 template <int ROWS, int BM, int LD, int MAXKS>
 __device__ __forceinline__ void push_owner_sum(const float *red, const float *recv, int rank, int ks,
-                                               int n0, int m0, int M, int N, void *y, int ybf16) {
+                                               int n0, int m0, int M, int N, void *y, int ybf16,
+                                               int *status) {
   const int lrows = log2_pow2(ROWS) - log2_pow2(ks), rows = 1 << lrows;
   const int lo = rank * rows;
   for (int e = threadIdx.x; e < rows * (BM / 4); e += blockDim.x) {
@@ -316,7 +317,8 @@ __device__ __forceinline__ void push_owner_sum(const float *red, const float *re
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int m = 4 * c4 + t;
-      if (m0 + m < M) store_y(y, static_cast<size_t>(m0 + m) * N + n0 + lo + i, vv[t], ybf16);
+      if (m0 + m < M && W4A16_IN_BOUNDS(m0 + m >= 0 && n0 + lo + i >= 0, status))
+        store_y(y, static_cast<size_t>(m0 + m) * N + n0 + lo + i, vv[t], ybf16);
     }
   }
 }

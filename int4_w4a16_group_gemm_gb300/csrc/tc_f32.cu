@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
       for (int i = 0; i < 4; ++i) w[i] = 0x88888888u;
       const int w0 = kb * 8 + apart * 4;
       if (!nvalid || kb >= kb1 || w0 >= Kw) return;
+      if (!W4A16_IN_BOUNDS(n < p.N && w0 >= 0, p.status)) return;
       if (w0 + 4 <= Kw) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qrow + w0));
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
@@ -360,6 +361,8 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
           uint4 o1, o2, o3;
           split_chunk(v, o1, o2, o3);
           const uint32_t off = sw128_offset(bm, chunk);
+          // the three 16-byte pieces inside the stage's three B tiles
+          (void)W4A16_IN_BOUNDS(off + 16u <= static_cast<uint32_t>(FX_B_BYTES), p.status);
           *reinterpret_cast<uint4 *>(st + off) = o1;
           *reinterpret_cast<uint4 *>(st + FX_B_BYTES + off) = o2;
           *reinterpret_cast<uint4 *>(st + 2 * FX_B_BYTES + off) = o3;
@@ -385,6 +388,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
 #pragma unroll
     for (int m = 0; m < FX_BM; ++m) acc[m] = 0.f;
     const int g_begin = 2 * kb0, g_end = min(G32, 2 * kb1);
+    (void)W4A16_IN_BOUNDS(!nvalid || g_end == g_begin || ((g_end - 1) >> gsh) < G, p.status);
     float s_next = (nvalid && g_begin < g_end) ? __ldg(srow + (g_begin >> gsh)) : 0.f;
     bool ok = true;
     for (int gk = g_begin, g = 0; gk < g_end; ++gk, ++g) {
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
   cluster_arrive();  // phase B: the slices of this rank's rows have landed
   if (*reinterpret_cast<volatile int *>(abort_flag) == 0)
     push_owner_sum<FX_ROWS, FX_BM, FX_RED_LD, FX_MAX_KS>(red, recv, rank, ks, n0, 0, p.M, p.N, p.y,
-                                                         p.ybf16);
+                                                         p.ybf16, p.status);
   cluster_wait();  // phase B: every slice this CTA sent has landed
   if (warp == 1) {
     tc_fence_after();

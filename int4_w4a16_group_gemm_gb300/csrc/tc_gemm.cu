@@ -270,7 +270,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
 #pragma unroll
         for (int h = 0; h < PIECES; ++h) {
           const int w0 = kb * 8 + part * WPT + PW * h;  // first word of this piece
-          if (w0 < Kw) {
+          if (w0 < Kw && W4A16_IN_BOUNDS(n < p.N && w0 + PW <= Kw && ((w0 * 8) >> p.gs) < G,
+                                         p.status)) {
             const uint32_t *src = reinterpret_cast<const uint32_t *>(qrow) + w0;
             if (PW == 4) {
               const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
@@ -319,6 +320,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           for (int j = 0; j < SK; ++j) {
             if (j < nsub) {
               uint8_t *arow = smem + (s * SK + j) * SB + row_off;
+              // this row's 128 bytes of the stage's A region
+              (void)W4A16_IN_BOUNDS(row_off + 128u <= static_cast<uint32_t>(Cfg::kABytes), p.status);
 #pragma unroll
               for (int i = 0; i < WPT; ++i) {
                 const int chunk = part * WPT + i;
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           if (ne < p.N) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (mb + j < p.M)
+              if (mb + j < p.M && W4A16_IN_BOUNDS(ne >= 0 && ne < p.N, p.status))
                 store_y(p.y, static_cast<size_t>(mb + j) * p.N + ne, __uint_as_float(r[j]),
                         p.ybf16);
           }

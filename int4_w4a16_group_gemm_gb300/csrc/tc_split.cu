@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int w0 = kb * 8 + 4 * h;
-        if (w0 < Kw) sc[h] = __ldg(srow + ((w0 * 8) >> p.gs));  // 32 columns, one group
+        if (w0 < Kw && W4A16_IN_BOUNDS(((w0 * 8) >> p.gs) < G, p.status))
+          sc[h] = __ldg(srow + ((w0 * 8) >> p.gs));  // 32 columns, one group
       }
     };
     // this row's 16-byte chunks 2j and 2j+1 in a weight stage (row r at
@@ -287,6 +288,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const uint32_t wsw = static_cast<uint32_t>(row & 7);
     const uint32_t woff0 = static_cast<uint32_t>(row * 128) + (((2u * j) ^ wsw) << 4);
     const uint32_t woff1 = static_cast<uint32_t>(row * 128) + (((2u * j + 1u) ^ wsw) << 4);
+    (void)W4A16_IN_BOUNDS(woff0 + 16u <= static_cast<uint32_t>(SP_W_BYTES) &&
+                              woff1 + 16u <= static_cast<uint32_t>(SP_W_BYTES),
+                          p.status);
     float rsc[2][2];
     fetch_sc(kb0 + j, rsc[0]);
     fetch_sc(kb0 + SP_SK + j, rsc[1]);
@@ -322,8 +326,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           const float *srow_s = reinterpret_cast<const float *>(wst + SP_W_BYTES) + row * p.scb;
           const int c0g = ((kbs * SP_BK) >> p.gs) & ~3;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            cs[h] = srow_s[((((kbs + j) * SP_BK) + 32 * h) >> p.gs) - c0g];
+          for (int h = 0; h < 2; ++h) {
+            const int off = ((((kbs + j) * SP_BK) + 32 * h) >> p.gs) - c0g;
+            cs[h] = W4A16_IN_BOUNDS(off >= 0 && off < p.scb, p.status) ? srow_s[off] : 0.f;
+          }
         }
         tc_fence_after();
         if (kbs + j < kb1) {
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   cluster_arrive();  // phase B: the slices of this rank's rows have landed
   if (*reinterpret_cast<volatile int *>(abort_flag) == 0)
     push_owner_sum<SP_ROWS, SP_BM, SP_RED_LD, SP_MAX_KS>(red, recv, rank, ks, n0, m0, p.M, p.N,
-                                                         p.y, p.ybf16);
+                                                         p.y, p.ybf16, p.status);
   cluster_wait();  // phase B: every slice this CTA sent has landed
   if (warp == 1) {
     tc_fence_after();

@@ -44,7 +44,19 @@ def test_library_exports_every_declared_symbol(w4):
 def test_status_strings(w4):
     assert w4.status_string(0) == "W4A16_OK"
     assert w4.status_string(5) == "W4A16_ERR_TIMEOUT"
+    assert w4.status_string(6) == "W4A16_ERR_BOUNDS"
     assert w4.status_string(99) == "W4A16_ERR_UNKNOWN"
+
+
+def test_bounds_checking_build_compiles_and_exports_the_boundary():
+    """The W4A16_DEBUG build (kernels check their indices and record
+    W4A16_ERR_BOUNDS) compiles from the same sources and exports every
+    declared entry point; its GPU test runs the shapes through it."""
+    from int4_w4a16_group_gemm_gb300 import build
+    path = build.build(debug=True)
+    lib = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} not exported by the checked build"
 
 
 def test_host_argument_checks_need_no_gpu(w4):
