@@ -105,6 +105,19 @@ void moe_workspace_offsets(int T, int topk, int E, int H, int I, size_t *off_per
                            size_t *off_o);
 // `shared_o` ([T][H] fp32, or nullptr) is added to every token's output
 // after its routed slots (the shared expert's output).
+// Tensor-core expert GEMMs of the MoE layer (moe_tc.cu): bf16 activations,
+// n_pairs >= 16, H and I multiples of 256, scale rows whole 16-byte units.
+bool moe_tc_supported(int n_pairs, int H, int I, int group);
+// xs[s] = x[perm[s] / topk] (bf16 rows of H).
+cudaError_t launch_moe_gather(const uint16_t *x, const int32_t *perm, int n, int topk, int H,
+                              uint16_t *xs, cudaStream_t stream);
+// One expert GEMM over the work items of the sort (token tiles of 16):
+// mode 0 gate/up + SwiGLU -> h (bf16, by sorted position) from xs; mode 1
+// down x routing weight -> o (fp32, by pair) from h.
+cudaError_t launch_moe_tc(int mode, const uint16_t *b, const int32_t *qw, const float *sc,
+                          const int32_t *offsets, const int32_t *items, const int32_t *n_items,
+                          const int32_t *perm, const float *route_w, int n_pairs, int E, int H,
+                          int I, int group, int max_items, void *out, cudaStream_t stream);
 cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const float *route_w,
                        int T, int topk, const int32_t *qw_gu, const float *sc_gu,
                        const int32_t *qw_dn, const float *sc_dn, int E, int H, int I,

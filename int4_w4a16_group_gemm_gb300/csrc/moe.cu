@@ -526,6 +526,32 @@ cudaError_t launch_moe(const void *x, bool x_bf16, const int32_t *ids, const flo
   void *h = ws + L.off_h;
   float *o = reinterpret_cast<float *>(ws + L.off_o);
   const int n = T * topk;
+  // bf16 activations at sizes the tensor-core expert kernels take: the same
+  // sort with token tiles of 16, the activation rows gathered in sorted
+  // order (into the o region, which the down GEMM overwrites afterwards),
+  // then both expert GEMMs on the tensor cores (moe_tc.cu)
+  if (x_bf16 && moe_tc_supported(n, H, I, group)) {
+    const int tc_tile = 16;
+    const int tc_items = moe_max_items(n, E, tc_tile);
+    moe_sort_kernel<<<1, 1024, 0, stream>>>(ids, n, E, offsets, perm, tc_tile, items, n_items,
+                                            di.status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(o);
+    err = launch_moe_gather(static_cast<const uint16_t *>(x), perm, n, topk, H, xs, stream);
+    if (err != cudaSuccess) return err;
+    err = launch_moe_tc(0, xs, qw_gu, sc_gu, offsets, items, n_items, perm, route_w, n, E, H, I,
+                        group, tc_items, h, stream);
+    if (err != cudaSuccess) return err;
+    err = launch_moe_tc(1, static_cast<const uint16_t *>(h), qw_dn, sc_dn, offsets, items, n_items,
+                        perm, route_w, n, E, H, I, group, tc_items, o, stream);
+    if (err != cudaSuccess) return err;
+    const long long work = static_cast<long long>(T) * (H / 4);
+    const int grid = static_cast<int>(std::min<long long>((work + 255) / 256, di.num_sms * 8ll));
+    moe_combine_kernel<<<std::max(grid, 1), 256, 0, stream>>>(o, ids, shared_o, T, topk, H, E, y,
+                                                              di.status);
+    return cudaGetLastError();
+  }
   const int tile = moe_tile(H, I);
   const int max_items = moe_max_items(n, E, tile);
 
