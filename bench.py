@@ -529,14 +529,15 @@ class MoeBlockWorkload(Workload):
         return self.bytes / per_call / 1e12, desc
 
 
-def make_workloads(keys, w4, torch, dev, overlap=True, moe_experts=MOE_E, moe_tokens=MOE_T):
+def make_workloads(keys, w4, torch, dev, overlap=True, moe_experts=MOE_E, moe_tokens=MOE_T,
+                   algo="auto"):
     out = {}
     moe = None
     for key in keys:
         if key in GEMM_SPECS:
             M, N, K, dt, seed, outlier, name = GEMM_SPECS[key]
-            out[key] = GemmWorkload(w4, torch, dev, M, N, K, dt, seed, outlier, overlap=overlap,
-                                    name=name)
+            out[key] = GemmWorkload(w4, torch, dev, M, N, K, dt, seed, outlier, algo=algo,
+                                    overlap=overlap, name=name)
         elif key in ("2-f32", "2-bf16"):
             out[key] = PairWorkload(w4, torch, dev, key.split("-")[1], overlap=overlap)
         elif key in ("3", "5"):
@@ -805,7 +806,8 @@ def run_ours(args):
     if sampler:
         sampler.start()
     wls = make_workloads([head], w4, torch, dev, overlap=not args.no_overlap,
-                         moe_experts=args.moe_experts, moe_tokens=args.moe_tokens)
+                         moe_experts=args.moe_experts, moe_tokens=args.moe_tokens,
+                         algo=args.algo)
     wl = wls[head]
     res = measure(torch, wl, args, stream, pk, world, e2e_steps=min(args.steps, args.e2e_steps),
                   cpu_budget=None)
@@ -821,7 +823,8 @@ def run_ours(args):
         "dtype": wl.dtype,
         "data": "synthetic (seeded: x ~ N(0,1), W ~ N(0,1/K) quantised on the device)",
         "config": {**workload_config(head, args.moe_experts, args.moe_tokens),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"algo": args.algo} if args.algo != "auto" else {})},
         "timing": {"method": ("one CUDA graph of K steps, replayed once; stream held by a spin "
                               "kernel before the start event (host enqueue time not counted)"),
                    "overlap": not args.no_overlap, "us_per_call": res["us_per_call"],
@@ -843,7 +846,8 @@ def run_ours(args):
     if extra:
         configs = {}
         others = make_workloads(extra, w4, torch, dev, overlap=not args.no_overlap,
-                                moe_experts=args.moe_experts, moe_tokens=args.moe_tokens)
+                                moe_experts=args.moe_experts, moe_tokens=args.moe_tokens,
+                                algo=args.algo)
         csampler = ClockSampler(local)
         csampler.start()
         for key in extra:
@@ -885,6 +889,9 @@ def main():
     ap.add_argument("--moe-experts", type=int, default=MOE_E,
                     help="experts of the MoE workloads (configs 3 and 5); fewer only to profile "
                          "the same kernels on a smaller working set")
+    ap.add_argument("--algo", default="auto", choices=["auto", "stream", "gemv", "tc"],
+                    help="GEMM kernel of the single-GEMM workloads (configs 0, 1, 4); auto "
+                         "is the library's own choice")
     ap.add_argument("--moe-tokens", type=int, default=MOE_T,
                     help="tokens of the MoE workloads (configs 3 and 5); see --moe-experts")
     args = ap.parse_args()

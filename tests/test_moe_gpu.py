@@ -156,10 +156,14 @@ def test_small_moe(w4, bf16, T, H, I, E, topk):
 
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("group", [64, 128])
-@pytest.mark.parametrize("T,H,I,E,topk", [(5, 256, 128, 6, 2), (16, 1024, 384, 9, 4)])
+@pytest.mark.parametrize("T,H,I,E,topk", [(5, 256, 128, 6, 2), (16, 1024, 384, 9, 4),
+                                          (16, 1024, 512, 9, 4), (100, 768, 512, 5, 3)])
 def test_small_moe_group_sizes(w4, bf16, group, T, H, I, E, topk):
     """Groups of 64 and 128 on both expert GEMMs; I = 384 with group 128
-    gives 3 scales per down-projection row (loaded per lane, not staged)."""
+    gives 3 scales per down-projection row (loaded per lane, not staged).
+    The last two shapes take the tensor-core expert GEMMs in bf16 mode
+    (H and I multiples of 256, at least 16 pairs); the last gives experts
+    several 16-token tiles with a ragged final one."""
     seed = T + H + E + group
     x = synth.activations(seed, T, H)
     ids, rw = synth.routing(seed, T, topk, E)
