@@ -10,14 +10,15 @@
 //     three 8-bit pieces);
 //   * (nib - 8) is a small integer, exact in bf16.
 // The products (nib - 8) * x_i are exact, the tensor cores add them in fp32
-// into TMEM, one 32-column group at a time (one MMA per 16 columns with the
-// three pieces side by side as N = 192) into a ring of two accumulators,
-// readback warps add the three pieces' sums in fp32, multiply each group's
-// sum by its fp32 scale and accumulate in registers. The scale never passes
-// through bf16, so the result carries only fp32 summation error. The depth
-// per output is the 32 columns of a group inside the tensor core, the
-// CTA's groups (an fp32 FMA chain, at most 128 for K <= 16384), then the
-// split-K partials of the cluster in rank order.
+// into TMEM, one 32-column group at a time: per 16 columns one MMA of N = 64
+// for each piece, all three into the group's accumulator, in a ring of six
+// accumulators (so the MMAs run up to five groups ahead of the readback);
+// readback warps multiply each group's sum by its fp32 scale and accumulate
+// in registers. The scale never passes through bf16, so the result carries
+// only fp32 summation error. The depth per output is the 6 MMAs of a
+// 32-column group inside the tensor core, the CTA's groups (an fp32 FMA
+// chain, at most 128 for K <= 16384), then the split-K partials of the
+// cluster in rank order.
 //
 // Tile: 128 weight rows x 64 tokens; K is split over a cluster of up to 4
 // CTAs exactly as in the bf16 small-M kernel, whose cluster reduction this
@@ -75,8 +76,8 @@ constexpr int FX_STAGE = 3 * FX_B_BYTES;        // one MMA stage in shared memor
 constexpr int FX_NS = 4;            // MMA stages
 constexpr int FX_NSX = 3;           // fp32 activation tiles in flight
 constexpr int FX_PD = 2;            // stages of packed weights prefetched per thread
-constexpr int FX_NB = 3 * FX_BM;    // MMA N: the three activation pieces side by side
-constexpr int FX_ACC = 2;           // group accumulators in TMEM (FX_NB columns each)
+constexpr int FX_NB = FX_BM;        // MMA N: the tile's tokens
+constexpr int FX_ACC = 6;           // group accumulators in TMEM (FX_NB columns each)
 constexpr int FX_TMEM_COLS = 512;   // the accumulators, then the A ring
 constexpr int FX_A_COL0 = FX_ACC * FX_NB;  // A stage s at column FX_A_COL0 + 32 s
 static_assert(FX_A_COL0 + FX_NS * 32 <= FX_TMEM_COLS, "TMEM budget");
@@ -86,7 +87,7 @@ constexpr int FX_RECV_BYTES = push_recv_bytes<FX_ROWS, FX_RED_LD, FX_MAX_KS>();
 constexpr int FX_SMEM = FX_NS * FX_STAGE + FX_NSX * FX_X_BYTES + FX_RECV_BYTES + 1024 + 256;
 static_assert(FX_ROWS * FX_RED_LD * 4 <= FX_NS * FX_STAGE, "parked partial tile");
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
-// N = 192 (the three 64-row piece tiles are one K-major B tile), M = 128.
+// N = 64 (one piece tile), M = 128.
 constexpr uint32_t FX_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                               (static_cast<uint32_t>(FX_NB >> 3) << 17) |
                               (static_cast<uint32_t>(FX_ROWS >> 4) << 24);
@@ -266,11 +267,15 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
           break;
         }
         tc_fence_after();
-        // one MMA per 16 columns covers the three pieces: A is read once
+        // the three pieces' products go into the same accumulator (piece
+        // tile p starts FX_B_BYTES / 16 units further in the start field)
 #pragma unroll
-        for (int k = 0; k < 2; ++k)  // +32 bytes per K step: +2 in the start field
-          tc_mma_tmem_a_warp(tmem + buf * FX_NB, a0 + (2 * h + k) * 8, b0 + 2 * (2 * h + k),
-                             FX_IDESC, k > 0 ? 1u : 0u);
+        for (int pc = 0; pc < 3; ++pc)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)  // +32 bytes per K step: +2 in the start field
+            tc_mma_tmem_a_warp(tmem + buf * FX_NB, a0 + (2 * h + k) * 8,
+                               b0 + pc * (FX_B_BYTES >> 4) + 2 * (2 * h + k), FX_IDESC,
+                               (pc > 0 || k > 0) ? 1u : 0u);
         tc_commit_warp(&acc_full[buf]);
         issued_any = true;
       }
@@ -402,21 +407,14 @@ __global__ void __launch_bounds__(FX_THREADS, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * FX_NB;
-      // the group sum is the three pieces' sums added in fp32
+      // the group sum (all three pieces) times the group scale
 #pragma unroll
       for (int part = 0; part < FX_BM / 16; ++part) {
         uint32_t d[16];
-        float t[16];
         tmem_ld_16cols(taddr + part * 16, d);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = __uint_as_float(d[j]);
-        tmem_ld_16cols(taddr + FX_BM + part * 16, d);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] += __uint_as_float(d[j]);
-        tmem_ld_16cols(taddr + 2 * FX_BM + part * 16, d);
-#pragma unroll
         for (int j = 0; j < 16; ++j)
-          acc[part * 16 + j] = fmaf(s, t[j] + __uint_as_float(d[j]), acc[part * 16 + j]);
+          acc[part * 16 + j] = fmaf(s, __uint_as_float(d[j]), acc[part * 16 + j]);
       }
       tc_fence_before();
       __syncwarp();
