@@ -12,18 +12,21 @@
 //
 // Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: 2-D tiled loads of x (128-byte swizzle) into
-//               the B slot of each pipeline stage;
+//               the B slot and of the packed words into the W slot of each
+//               pipeline stage;
 //   warp 1      TMEM owner and MMA issuer: the warp runs the issue loop
 //               and one elected lane issues tcgen05.mma (kind::f16, bf16 x
 //               bf16 -> f32) per 16-wide K step and commits each stage back
 //               to its producers;
-//   warps 2-9   dequantisers: thread r owns weight row r of the tile, loads
-//               its packed words and scales straight from global memory,
-//               forms fp32 (nibble - 8) * scale exactly, rounds to bf16 and
-//               stores the 16-byte chunks in the canonical K-major 128-byte
-//               swizzled layout the MMA reads; after a tile's last stage
-//               the same warps drain the accumulators (tcgen05.ld) to y.
-// Stage = 64 K columns: A 2 x 16 KB (dequantised) + B 32 KB (TMA); 3 stages.
+//   warps 2-9   dequantisers: thread r owns weight row r of the tile, reads
+//               its packed words from the stage (TMA) and loads its scales
+//               from global memory two stages ahead, forms fp32
+//               (nibble - 8) * scale exactly, rounds to bf16 and stores the
+//               16-byte chunks in the canonical K-major 128-byte swizzled
+//               layout the MMA reads; after a tile's last stage the same
+//               warps drain the accumulators (tcgen05.ld) to y.
+// Stage = 64 K columns: A 2 x 16 KB (dequantised) + B 32 KB (TMA) + the
+// packed words 8 KB (TMA, one 8-word x 256-row box); 3 stages.
 // Every wait is bounded; a timeout is recorded in the status word and the
 // CTA unwinds (TMEM is always freed).
 //
@@ -62,16 +65,19 @@ struct TcCfg {
   static constexpr int kRows = 128 * SUBS;                 // weight rows per tile
   static constexpr int kABytes = SUBS * A_SUB_BYTES;
   static constexpr int kBBytes = BM * TC_BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kWBytes = kRows * TC_BK / 2;  // the stage's packed words (TMA)
+  static constexpr int kStageBytes = kABytes + kBBytes + kWBytes;
   static constexpr int kBlocks = 3;   // 64-column blocks in the ring
   // blocks per pipeline stage (one barrier handshake per stage); a stage of
   // this tile already carries 16 MMAs of N = 256
   static constexpr int kSubK = 1;
   static constexpr int kStages = kBlocks / kSubK;
-  static constexpr int kPrefetch = 1;  // stages of packed weights in flight per thread
+  static constexpr int kPrefetch = 2;  // stages of scales in flight per thread
   static constexpr int kThreadsPerRow = 32 * kDqWarps / kRows;  // dequant threads per row
   static constexpr int kTmemCols = SUBS * BM < 32 ? 32 : SUBS * BM;  // a power of two
   static constexpr int kSmem = kBlocks * kStageBytes + 1024 + 256;
+  static_assert(kSubK == 1, "one 64-column block per stage (one packed-word box)");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
   // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
   // 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
   // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -95,7 +101,8 @@ struct TcParams {
 // all of K.
 template <int BM, int SUBS>
 __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
   using Cfg = TcCfg<BM, SUBS>;
   constexpr int NS = Cfg::kStages;
   constexpr int SK = Cfg::kSubK;       // 64-column blocks per stage
@@ -112,7 +119,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * SK * SB);
   uint64_t *empty = full + NS;
-  uint64_t *acc_full = empty + NS;
+  uint64_t *wfull = empty + NS;  // [NS] the stage's packed words have landed
+  uint64_t *acc_full = wfull + NS;
   uint64_t *acc_empty = acc_full + 1;
   uint64_t *drain = acc_empty + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -129,6 +137,7 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1 + DQ_WARPS);
       mbar_init(&empty[s], 1);
+      mbar_init(&wfull[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, DQ_WARPS);
@@ -169,16 +178,19 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
       int it = 0;
       for (int tile = tile_first; tile < p.num_tiles && !aborted(abort_flag); tile += tile_step) {
         const int m0 = (tile % p.tiles_m) * BM;
+        const int n0 = (tile / p.tiles_m) * ROWS;
         for (int kb = kb0; kb < kb1; kb += SK, ++it) {
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
-          const int nsub = min(SK, kb1 - kb);
           if (!mbar_wait(&empty[s], ph ^ 1u)) { fail(); break; }
           if (aborted(abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * Cfg::kBBytes));
-          for (int j = 0; j < nsub; ++j)
-            tma_load_2d_hint(smem + (s * SK + j) * SB + Cfg::kABytes, &tmap_x, (kb + j) * TC_BK,
-                             m0, &full[s], keep);
+          uint8_t *st = smem + s * SB;
+          // the packed words of the tile's rows (one 8-word x ROWS box, zeros
+          // past K and N), then the activation tile
+          mbar_arrive_expect_tx(&wfull[s], static_cast<uint32_t>(Cfg::kWBytes));
+          tma_load_2d(st + Cfg::kABytes + Cfg::kBBytes, &tmap_w, kb * 8, n0, &wfull[s]);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(Cfg::kBBytes));
+          tma_load_2d_hint(st + Cfg::kABytes, &tmap_x, kb * TC_BK, m0, &full[s], keep);
         }
       }
     }
@@ -245,6 +257,8 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
     const uint32_t row_off =
         static_cast<uint32_t>(sub * A_SUB_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
     const int swz = rr & 7;
+    // this thread's words inside a stage's packed-word box
+    (void)W4A16_IN_BOUNDS(row * (TC_BK / 2) + (part + 1) * WPT * 4 <= Cfg::kWBytes, p.status);
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
     const int esub = (warp - 2) >> 2;        // accumulator this warp drains
     int it = 0, tcount = 0;
@@ -254,42 +268,28 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
       const int m0 = (tile % p.tiles_m) * BM;
       const int n = n0 + row;
       const bool nvalid = n < p.N;
-      const uint4 *qrow = reinterpret_cast<const uint4 *>(p.qw + static_cast<size_t>(n) * Kw);
       const float *srow = p.sc + static_cast<size_t>(n) * G;
 
-      // register ring of PD prefetched stages (slots indexed at compile time);
-      // each stage of this thread: SK blocks of WPT words and their scale(s)
-      uint32_t ra[PD][SK][WPT];
+      // register ring of PD prefetched stages of scales (slots indexed at
+      // compile time); the packed words come by TMA with the stage
       float rs[PD][SK][PIECES];
-      auto fetch = [&](int kb, uint32_t (&w)[WPT], float (&sc)[PIECES]) {
-#pragma unroll
-        for (int i = 0; i < WPT; ++i) w[i] = 0u;
+      auto fetch = [&](int kb, float (&sc)[PIECES]) {
 #pragma unroll
         for (int h = 0; h < PIECES; ++h) sc[h] = 0.f;
         if (!nvalid || kb >= kb1) return;
 #pragma unroll
         for (int h = 0; h < PIECES; ++h) {
           const int w0 = kb * 8 + part * WPT + PW * h;  // first word of this piece
+          // a piece past K keeps scale 0 (its zero-filled words then weigh 0)
           if (w0 < Kw && W4A16_IN_BOUNDS(n < p.N && w0 + PW <= Kw && ((w0 * 8) >> p.gs) < G,
-                                         p.status)) {
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(qrow) + w0;
-            if (PW == 4) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
-              w[4 * h] = v.x; w[4 * h + 1] = v.y; w[4 * h + 2] = v.z; w[4 * h + 3] = v.w;
-            } else if (PW == 2) {
-              const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src));
-              w[0] = v.x; w[1] = v.y;
-            } else {
-              w[0] = __ldg(src);
-            }
+                                         p.status))
             sc[h] = __ldg(srow + ((w0 * 8) >> p.gs));  // a piece lies in one group
-          }
         }
       };
 #pragma unroll
       for (int u = 0; u < PD; ++u)
 #pragma unroll
-        for (int j = 0; j < SK; ++j) fetch(kb0 + u * SK + j, ra[u][j], rs[u][j]);
+        for (int j = 0; j < SK; ++j) fetch(kb0 + u * SK + j, rs[u][j]);
       bool ok = true;
       // one stage (SK blocks) per iteration: the SK blocks' words are
       // independent, so their dequantisation interleaves
@@ -302,20 +302,37 @@ __global__ void __launch_bounds__(TcCfg<BM, SUBS>::kThreads, 1)
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           ++it;
-          uint32_t cw[SK][WPT];
           float cs[SK][PIECES];
 #pragma unroll
-          for (int j = 0; j < SK; ++j) {
-#pragma unroll
-            for (int i = 0; i < WPT; ++i) cw[j][i] = ra[u][j][i];
+          for (int j = 0; j < SK; ++j)
 #pragma unroll
             for (int h = 0; h < PIECES; ++h) cs[j][h] = rs[u][j][h];
-          }
 #pragma unroll
-          for (int j = 0; j < SK; ++j) fetch(kbs + PD * SK + j, ra[u][j], rs[u][j]);
+          for (int j = 0; j < SK; ++j) fetch(kbs + PD * SK + j, rs[u][j]);
+          // the stage's packed words have landed (the producer loads them
+          // once the stage's previous MMAs are complete, so its A region is
+          // free too)
           const bool got =
-              __all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u) && !aborted(abort_flag));
+              __all_sync(0xFFFFFFFFu, mbar_wait(&wfull[s], ph) && !aborted(abort_flag));
           if (!got) { fail(); ok = false; break; }
+          uint32_t cw[SK][WPT];
+#pragma unroll
+          for (int j = 0; j < SK; ++j) {
+            const uint8_t *wrow = smem + (s * SK + j) * SB + Cfg::kABytes + Cfg::kBBytes +
+                                  row * (TC_BK / 2) + part * WPT * 4;
+#pragma unroll
+            for (int h = 0; h < PIECES; ++h) {
+              if (PW == 4) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(wrow + 16 * h);
+                cw[j][4 * h] = v.x; cw[j][4 * h + 1] = v.y; cw[j][4 * h + 2] = v.z;
+                cw[j][4 * h + 3] = v.w;
+              } else {
+#pragma unroll
+                for (int i = 0; i < PW; ++i)
+                  cw[j][PW * h + i] = reinterpret_cast<const uint32_t *>(wrow)[PW * h + i];
+              }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < SK; ++j) {
             if (j < nsub) {
@@ -384,8 +401,8 @@ bool tc_gemm_supported(int M, int N, int K) {
 namespace {
 
 template <int BM, int SUBS>
-cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, bool overlap,
-                      cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap &tmap, const CUtensorMap &tmap_w, const TcParams &p,
+                      int grid_x, bool overlap, cudaStream_t stream) {
   using Cfg = TcCfg<BM, SUBS>;
   auto kern = tc_gemm_kernel<BM, SUBS>;
   static PerDeviceOnce attr_once;
@@ -403,7 +420,7 @@ cudaError_t launch_tc(const CUtensorMap &tmap, const TcParams &p, int grid_x, bo
   attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, p);
 }
 
 int env_int(const char *name) {
@@ -444,6 +461,16 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // packed words [N][K/8]: 8 words (one 64-column block) x ROWS rows per box,
+  // zeros past K and N
+  CUtensorMap tmap_w;
+  const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
+  const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
+  const cuuint32_t wbox[2] = {TC_BK / 8, static_cast<cuuint32_t>(ROWS)};
+  r = encode(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<int32_t *>(qw), wdims,
+             wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   TcParams p{};
   p.qw = qw;
   p.sc = sc;
@@ -456,7 +483,7 @@ cudaError_t launch_tc_gemm(const uint16_t *x, const int32_t *qw, const float *sc
   p.num_tiles = p.tiles_m * ((N + ROWS - 1) / ROWS);
   p.gs = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.status = di.status;
-  return launch_tc<BM, 2>(tmap, p, std::min(p.num_tiles, di.num_sms), overlap, stream);
+  return launch_tc<BM, 2>(tmap, tmap_w, p, std::min(p.num_tiles, di.num_sms), overlap, stream);
 }
 
 }  // namespace w4a16
