@@ -171,6 +171,17 @@ def test_small_moe_group_sizes(w4, bf16, group, T, H, I, E, topk):
     check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, bf16, group)
 
 
+@pytest.mark.parametrize("T,topk,E,H,I", [(4, 4, 4, 256, 256), (2, 8, 8, 512, 256)])
+def test_moe_tensor_core_path_smallest(w4, T, topk, E, H, I):
+    """Exactly 16 (token, slot) pairs (the fewest the tensor-core expert path
+    takes) in bf16 mode, H and I at their 256 minimum or just above: every
+    expert has a single, partly filled 16-token tile."""
+    x = synth.activations(T * 7 + E, T, H)
+    ids, rw = synth.routing(T * 7 + E, T, topk, E)
+    qgu, sgu, qdn, sdn = build_experts_host(T * 7 + E, E, H, I)
+    check_moe(w4, x, ids, rw, qgu, sgu, qdn, sdn, True)
+
+
 def test_moe_many_tokens_one_expert(w4):
     # every token routed to expert 0 in slot 0: its weights serve 37 tokens
     T, H, I, E, topk = 37, 512, 256, 3, 2
